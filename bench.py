@@ -1,0 +1,487 @@
+"""Benchmark of the sink-attention hot path on B300.
+
+Headline (the `value` of the JSON line): sliding-window sink-attention prefill,
+bf16, B=1, T=32768, Hq=64, Hkv=8, D=128, W=128, in TFLOP/s counting unmasked
+work only (4*D*Hq per visible (query, key) pair).  One step = one prefill call
+over that batch.  The same line carries `parts`: the global-attention prefill
+on the same shapes (TFLOP/s) and the MTP verify configurations (KV GB/s and
+calls/s): 64 requests x 4 tokens with contexts ~ U[4096, 65536] against the
+paged GA cache and the 131-slot SWA ring (39 SWA layers back to back), and
+8 requests at context 262144 with q_len in {1, 4}.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs under torchrun as independent replicas (weak scaling, no data-path
+collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sink-attn prefill TFLOP/s and MTP-verify KV GB/s, % of B300 roofline"
+B, T, HQ, HKV, D, W = 1, 32768, 64, 8, 128, 128
+QMAX, PAGE, RING = 4, 64, W + 4 - 1
+SWA_LAYERS = 39   # SWA layers of the 48-layer model (39 SWA + 9 GA)
+
+
+# ------------------------------------------------------------ workload math
+def visible_pairs(T_: int, window: int | None) -> int:
+    """Number of (query, key) pairs with 0 <= j <= i and (GA or j > i - W)."""
+    if window is None or window >= T_:
+        return T_ * (T_ + 1) // 2
+    return window * T_ - window * (window - 1) // 2
+
+
+def prefill_flop(T_: int, window: int | None) -> float:
+    return 4.0 * D * HQ * visible_pairs(T_, window) * B
+
+
+def prefill_min_bytes() -> float:
+    return 2.0 * (2 * B * T * HQ * D + 2 * B * T * HKV * D)   # Q, O, K, V once each (bf16)
+
+
+def verify_kv_bytes(ctx: np.ndarray) -> float:
+    """K+V bytes of the visible cache, read once per (request, kv head)."""
+    return float(np.sum(ctx.astype(np.float64))) * HKV * D * 2 * 2
+
+
+# ------------------------------------------------------------ host helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def source_sha(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_file: str, name: str):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(name)
+        if rec and rec.get("source_sha") == source_sha(kernel_file):
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (the timing rule); identity for one process."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ GPU timing
+def time_region(fn, steps: int, world: int, stream):
+    """CUDA-event time of `steps` calls of fn on `stream`, barrier + sync on both sides."""
+    import torch
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(stop) / steps
+
+
+def bench_prefill(A, synth, kind: str, steps: int, warmup: int, world: int, stream, seed: int):
+    import torch
+    sets = []
+    for s in range(2):   # two rotating input sets; each set (1.2 GB) exceeds L2
+        q, k, v, sink = synth.prefill_inputs(B, T, HQ, HKV, D, seed + s, device="cuda")
+        sets.append((q, k, v, sink, torch.empty_like(q)))
+    window = W if kind == "swa" else None
+
+    def step(i):
+        q, k, v, sink, o = sets[i % 2]
+        if kind == "swa":
+            A.attn_swa_sink_prefill(q, k, v, sink, window=W, out=o, stream=stream)
+        else:
+            A.attn_ga_sink_prefill(q, k, v, sink, out=o, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+        ms = time_region(step, steps, world, stream)
+    if A.attn_check_device_error(stream) != 0:
+        raise RuntimeError(f"{kind} prefill reported a device error")
+    return ms, prefill_flop(T, window)
+
+
+def bench_prefill_e2e(A, synth, steps: int, warmup: int, world: int, stream, seed: int):
+    """Same metric through the public call with host buffers: every step copies
+    the inputs from pinned host memory and reads the output back."""
+    import torch
+    q, k, v, sink = synth.prefill_inputs(B, T, HQ, HKV, D, seed, device="cuda")
+    hq, hk, hv, hs = (x.cpu().pin_memory() for x in (q, k, v, sink))
+    ho = torch.empty_like(hq).pin_memory()
+    dq, dk, dv, ds, do = (torch.empty_like(x, device="cuda") for x in (hq, hk, hv, hs, ho))
+
+    def step(_):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ds.copy_(hs, non_blocking=True)
+        A.attn_swa_sink_prefill(dq, dk, dv, ds, window=W, out=do, stream=stream)
+        ho.copy_(do, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(1, warmup)):
+            step(i)
+        ms = time_region(step, steps, world, stream)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hs))
+    d2h = ho.numel() * ho.element_size()
+    return ms, h2d, d2h
+
+
+def _paged_problem(ctx, q_lens, seed, device="cuda"):
+    import torch
+    import synth
+    npages = (ctx + PAGE - 1) // PAGE
+    nb = len(ctx)
+    num_pages = int(npages.sum())
+    perm = synth.page_permutation(num_pages, seed)
+    pt = np.zeros((nb, int(npages.max())), np.int32)
+    o = 0
+    for b in range(nb):
+        pt[b, :npages[b]] = perm[o:o + npages[b]]
+        o += npages[b]
+    kp = synth.normal((num_pages, HKV, PAGE, D), seed + 1, device=device)
+    vp = synth.normal((num_pages, HKV, PAGE, D), seed + 2, device=device)
+    cu_q = synth.cu_seqlens(q_lens)
+    q = synth.normal((int(cu_q[-1]), HQ, D), seed + 3, device=device)
+    sink = synth.sink_logits(HQ, seed + 4, device=device)
+    return dict(kp=kp, vp=vp, pt=torch.from_numpy(pt).to(device), ctx=torch.from_numpy(ctx).to(device),
+                cu_q=torch.from_numpy(cu_q).to(device), q=q, sink=sink, max_ctx=int(ctx.max()))
+
+
+def bench_verify_ga(A, ctx, q_lens, steps, warmup, world, stream, seed):
+    import torch
+    P = _paged_problem(ctx, q_lens, seed)
+    ws_bytes = A.attn_ga_sink_verify_workspace(len(ctx), HQ, HKV, D, QMAX, P["max_ctx"])
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(P["q"])
+
+    def step(_):
+        A.attn_ga_sink_verify(P["q"], P["cu_q"], P["kp"], P["vp"], P["pt"], P["ctx"], P["sink"],
+                              max_ctx=P["max_ctx"], q_max=QMAX, out=out, workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+        ms = time_region(step, steps, world, stream)
+    if A.attn_check_device_error(stream) != 0:
+        raise RuntimeError("GA verify reported a device error")
+    return ms, verify_kv_bytes(ctx)
+
+
+def bench_verify_swa(A, nreq, steps, warmup, world, stream, seed):
+    """39 SWA layers back to back (distinct rings), replayed as one CUDA graph."""
+    import torch
+    import synth
+    rings = [(synth.normal((nreq, HKV, RING, D), seed + 2 * i, device="cuda"),
+              synth.normal((nreq, HKV, RING, D), seed + 2 * i + 1, device="cuda"))
+             for i in range(SWA_LAYERS)]
+    ctx = synth.context_lengths(nreq, 4096, 65536, seed + 99)
+    q_lens = np.full(nreq, QMAX, np.int32)
+    cu_q = torch.from_numpy(synth.cu_seqlens(q_lens)).cuda()
+    sl = torch.from_numpy(ctx).cuda()
+    q = synth.normal((nreq * QMAX, HQ, D), seed + 100, device="cuda")
+    sink = synth.sink_logits(HQ, seed + 101, device="cuda")
+    outs = [torch.empty_like(q) for _ in range(SWA_LAYERS)]
+
+    def layers():
+        for i, (rk, rv) in enumerate(rings):
+            A.attn_swa_sink_verify(q, cu_q, rk, rv, sl, sink, window=W, q_max=QMAX, out=outs[i],
+                                   stream=stream)
+
+    with torch.cuda.stream(stream):
+        layers()   # warm (tensor-map encode, function attributes)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            layers()
+        for _ in range(warmup):
+            graph.replay()
+        ms = time_region(lambda _: graph.replay(), steps, world, stream)
+    if A.attn_check_device_error(stream) != 0:
+        raise RuntimeError("SWA verify reported a device error")
+    kv = float(nreq) * RING * HKV * D * 2 * 2 * SWA_LAYERS
+    return ms, kv
+
+
+# --------------------------------------------------------------- CPU baseline
+def cpu_baseline(seconds_target: float = 15.0):
+    """The fp64 oracle on a bounded sample of the headline workload (rows of
+    the SWA prefill), timed on the host cores; value in unmasked TFLOP/s."""
+    import oracle
+    import synth
+    import torch
+    cores = len(os.sched_getaffinity(0))
+    q, k, v, sink = synth.prefill_inputs(B, T, HQ, HKV, D, 2024, dtype=torch.float32)
+    rng = np.random.default_rng(0)
+    n = 4096
+    total_rows, total_flop, total_s = 0, 0.0, 0.0
+    while total_s < seconds_target and total_rows < B * T * HQ:
+        rows = np.stack([np.zeros(n, np.int64), rng.integers(W, T, n), rng.integers(0, HQ, n)], 1)
+        t0 = time.perf_counter()
+        oracle.prefill_rows(q, k, v, sink, rows, W)
+        total_s += time.perf_counter() - t0
+        total_rows += n
+        total_flop += 4.0 * D * W * n   # rows past the first W see exactly W keys
+        n *= 2
+    return {"value": total_flop / total_s / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{total_rows} random rows (i >= W) of the SWA prefill, {total_s:.1f} s; "
+                      f"fp64 C loops, OpenMP over rows"}
+
+
+# --------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-parts", action="store_true", help="headline only")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    warmup = max(3, args.warmup)
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank, warmup)
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    import global_attention_sinks_swa_b300 as A
+    import synth
+    stream = torch.cuda.Stream()
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+
+    with ClockSampler(local) as clocks:
+        ms, flop = bench_prefill(A, synth, "swa", args.steps, warmup, world, stream, 1002 + 10 * rank)
+    ms_max = reduce_max(ms, world, torch.device("cuda", local))
+    value = world * flop / (ms_max * 1e-3) / 1e12
+    achieved = prefill_min_bytes() / (ms * 1e-3) / 1e9
+
+    parts = {}
+    launches = args.steps
+    if not args.no_parts:
+        steps_p = max(3, args.steps // 2)
+        ms_ga, flop_ga = bench_prefill(A, synth, "ga", steps_p, warmup, world, stream, 1003 + 10 * rank)
+        parts["ga_prefill"] = {"config": "B=1 T=32768 Hq=64 Hkv=8 D=128 full causal bf16",
+                               "value": flop_ga / (ms_ga * 1e-3) / 1e12, "unit": "TFLOP/s",
+                               "ms": ms_ga, "roofline": {"bound": "tensor",
+                                                         "peak": tf_burst, "unit": "TFLOP/s",
+                                                         "frac": flop_ga / (ms_ga * 1e-3) / 1e12 / tf_burst,
+                                                         "frac_sustained": flop_ga / (ms_ga * 1e-3) / 1e12 / tf_sus}}
+        ctx4 = synth.context_lengths(64, 4096, 65536, 1004)
+        ms4, kv4 = bench_verify_ga(A, ctx4, np.full(64, QMAX, np.int32), args.steps, warmup, world,
+                                   stream, 1004 + 10 * rank)
+        parts["verify_ga_64req"] = {"config": "64 req x q4, ctx~U[4096,65536], page 64",
+                                    "value": kv4 / (ms4 * 1e-3) / 1e9, "unit": "GB/s",
+                                    "calls_per_s": 1e3 / ms4, "ms": ms4,
+                                    "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                                                 "frac": kv4 / (ms4 * 1e-3) / 1e9 / hbm}}
+        ms_s, kv_s = bench_verify_swa(A, 64, args.steps, warmup, world, stream, 2004 + 10 * rank)
+        parts["verify_swa_64req_39layers"] = {
+            "config": "64 req x q4, 131-slot ring, 39 layers in one CUDA graph",
+            "value": kv_s / (ms_s * 1e-3) / 1e9, "unit": "GB/s", "calls_per_s": SWA_LAYERS * 1e3 / ms_s,
+            "ms_per_39_layers": ms_s,
+            "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                         "frac": kv_s / (ms_s * 1e-3) / 1e9 / hbm}}
+        for ql, name in ((4, "verify_ga_8x262144_q4"), (1, "verify_ga_8x262144_q1")):
+            ctx5 = np.full(8, 262144, np.int32)
+            ms5, kv5 = bench_verify_ga(A, ctx5, np.full(8, ql, np.int32), args.steps, warmup, world,
+                                       stream, 1005 + ql + 10 * rank)
+            parts[name] = {"config": f"8 req x q{ql}, ctx 262144, page 64",
+                           "value": kv5 / (ms5 * 1e-3) / 1e9, "unit": "GB/s",
+                           "calls_per_s": 1e3 / ms5, "ms": ms5,
+                           "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                                        "frac": kv5 / (ms5 * 1e-3) / 1e9 / hbm}}
+        torch.cuda.empty_cache()
+
+    e2e_ms, h2d, d2h = bench_prefill_e2e(A, synth, max(3, args.steps // 4), warmup, world, stream,
+                                         1002 + 10 * rank)
+    e2e_ms = reduce_max(e2e_ms, world, torch.device("cuda", local))
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": warmup,
+            "ms_per_step": ms_max,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic: Q,K,V ~ N(0,1) bf16, sink ~ N(0,1) fp32, seeded",
+            "config": {"workload": "SWA sink prefill B=1 T=32768 Hq=64 Hkv=8 D=128 W=128",
+                       "global_batch": B * world, "seq_len": T, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (1.2 GB per set, 2 rotating sets)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_source": peak_src,
+                         "traffic": ncu_traffic("global_attention_sinks_swa_b300/csrc/prefill_tc.cu",
+                                                "prefill_swa_kernel"),
+                         "algorithmic_bytes": prefill_min_bytes(),
+                         "tensor_frac": flop / (ms * 1e-3) / 1e12 / tf_burst},
+            "clocks": clocks.summary(),
+            "e2e": {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "parts": parts,
+        }
+        line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, world, rank, warmup):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    headline workload per step."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    import torch
+    q, k, v, sink = synth.prefill_inputs(B, T, HQ, HKV, D, 2024, dtype=torch.float32)
+    rng = np.random.default_rng(0)
+    n = 2048
+    def step():
+        rows = np.stack([np.zeros(n, np.int64), rng.integers(W, T, n), rng.integers(0, HQ, n)], 1)
+        oracle.prefill_rows(q, k, v, sink, rows, W)
+    for _ in range(warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 4.0 * D * W * n / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "SWA sink prefill B=1 T=32768 Hq=64 Hkv=8 D=128 W=128",
+                   "sample": f"{n} random rows per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} random rows (i >= W) of the SWA prefill per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    main()

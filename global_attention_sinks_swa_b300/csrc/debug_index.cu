@@ -1,0 +1,98 @@
+// Index dumps: replay the kernels' tile schedules and masks (the same
+// functions from index_math.cuh) and write integer results the tests compare
+// bit for bit with the definitions (visible iff 0 <= j <= i and, for SWA,
+// j >= i - W + 1; ring slot p mod R; page page_table[b][p / P]).
+#include "index_math.cuh"
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+// mode 0: GA tiling (two 128-row query tiles per CTA, key tiles of 128;
+// interior tiles admit every pair without a mask).  One thread per query row.
+__global__ void visits_ga_kernel(int32_t *visits, int T, int window) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= T) return;
+    const int qs = (i / kTileM) * kTileM;  // start of this row's query tile
+    int first, last;
+    ga_key_tiles(qs, T, window, &first, &last);
+    for (int j = first; j <= last; ++j) {
+        const bool masked = ga_tile_needs_mask(qs, j, window);
+        for (int c = 0; c < kTileN; ++c) {
+            const int kp = j * kTileN + c;
+            if (kp >= T) break;
+            if (!masked || key_visible(i, kp, window)) visits[static_cast<long>(i) * T + kp] += 1;
+        }
+    }
+}
+
+// mode 1: packed SWA tiling, G heads x 128/G tokens per tile; head 0 only.
+__global__ void visits_swa_kernel(int32_t *visits, int T, int window, int G) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= T) return;
+    const int TT = swa_pack_tokens(G);
+    const int i0 = (i / TT) * TT;
+    const int key0 = swa_pack_key0(i0, G, window), N = swa_pack_keys(G, window);
+    for (int c = 0; c < N; ++c) {
+        const int kp = key0 + c;
+        if (kp >= 0 && kp < T && key_visible(i, kp, window))
+            visits[static_cast<long>(i) * T + kp] += 1;
+    }
+}
+
+__global__ void verify_positions_kernel(int32_t *out, int kind, const int32_t *cu_q,
+                                        const int32_t *seq_lens, int q_max, int window, int R,
+                                        int max_pages, int page_size) {
+    const int b = blockIdx.x, t = blockIdx.y;
+    const int L = seq_lens[b], q_len = cu_q[b + 1] - cu_q[b];
+    const int i = L - q_len + t;  // query position
+    if (kind == 0) {
+        for (int s = threadIdx.x; s < R; s += blockDim.x) {
+            const int p = ring_slot_position(s, L, R);
+            out[(static_cast<long>(b) * q_max + t) * R + s] =
+                (t < q_len && p >= 0 && key_visible(i, p, window)) ? p : -1;
+        }
+    } else {
+        const long n = static_cast<long>(max_pages) * page_size;
+        int32_t *o = out + (static_cast<long>(b) * q_max + t) * n;
+        for (long x = threadIdx.x; x < n; x += blockDim.x) o[x] = -1;
+        __syncthreads();
+        if (t >= q_len) return;
+        const int nsplit = verify_num_splits(max_pages * page_size, kVerifyChunkPages * page_size);
+        for (int s = 0; s < nsplit; ++s) {
+            int pb, pe;
+            verify_split_pages(s, L, page_size, kVerifyChunkPages, &pb, &pe);
+            for (int pi = pb; pi < pe; ++pi)
+                for (int off = threadIdx.x; off < page_size; off += blockDim.x) {
+                    const int p = pi * page_size + off;
+                    if (key_visible(i, p, 0)) o[p] = p;
+                }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_debug_prefill_visits(int32_t *visits, int mode, int T, int window, int G,
+                                        cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    cudaError_t e = cudaMemsetAsync(visits, 0, sizeof(int32_t) * static_cast<size_t>(T) * T, s);
+    if (e != cudaSuccess) return e;
+    const int blocks = (T + 127) / 128;
+    if (mode == 0)
+        visits_ga_kernel<<<blocks, 128, 0, s>>>(visits, T, window);
+    else
+        visits_swa_kernel<<<blocks, 128, 0, s>>>(visits, T, window, G);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_verify_positions(int32_t *out, int kind, const int32_t *cu_q,
+                                          const int32_t *seq_lens, int B, int q_max, int window,
+                                          int R, int max_pages, int page_size, cudaStream_t s) {
+    if (B == 0 || q_max == 0) return cudaSuccess;
+    verify_positions_kernel<<<dim3(B, q_max), 128, 0, s>>>(out, kind, cu_q, seq_lens, q_max,
+                                                          window, R, max_pages, page_size);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

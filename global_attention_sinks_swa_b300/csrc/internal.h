@@ -1,0 +1,71 @@
+// Host-side interface between the C ABI (attn_api.cu) and the kernel files.
+// Each launcher only enqueues; argument validation happens in attn_api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// fp32 CUDA-core prefill (window <= 0: global attention).
+cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *sink,
+                               float *o, float *lse, int B, int T, int Hq, int Hkv, int D,
+                               int window, float scale, unsigned int *err, cudaStream_t s);
+
+// Tensor maps of a bf16 prefill problem (built by attn_api.cu).
+struct PrefillMaps {
+    CUtensorMap q;  // box rows of Q  (layout depends on the kernel)
+    CUtensorMap k;  // key tile
+    CUtensorMap v;  // value tile
+    CUtensorMap o;  // output store
+};
+
+// tcgen05 GA-tiled prefill (full causal, or window-limited when window > 0).
+cudaError_t launch_prefill_ga_tc(const PrefillMaps &maps, const float *sink, float *lse, int B,
+                                 int T, int Hq, int Hkv, int window, float scale,
+                                 unsigned int *err, cudaStream_t s);
+// tcgen05 packed-SWA prefill (G = Hq/Hkv heads x 128/G tokens per tile).
+cudaError_t launch_prefill_swa_tc(const PrefillMaps &maps, const float *sink, float *lse, int B,
+                                  int T, int Hq, int Hkv, int window, float scale,
+                                  unsigned int *err, cudaStream_t s);
+int prefill_swa_tc_supported(int G, int window);
+
+// KV-cache appends (plain 16-byte copies).
+cudaError_t launch_ring_append(const void *k_new, const void *v_new, const int32_t *cu_q,
+                               const int32_t *seq_lens, void *ring_k, void *ring_v, int B, int Hkv,
+                               int D, int R, int q_max, int elem_bytes, unsigned int *err,
+                               cudaStream_t s);
+cudaError_t launch_paged_append(const void *k_new, const void *v_new, const int32_t *cu_q,
+                                const int32_t *seq_lens, void *k_pages, void *v_pages,
+                                const int32_t *page_table, int max_pages, int num_pages,
+                                int page_size, int B, int Hkv, int D, int q_max, int elem_bytes,
+                                unsigned int *err, cudaStream_t s);
+
+// Verify (bf16, D = 128, mma.sync tensor cores, TMA-staged K/V).
+struct VerifyMaps {
+    CUtensorMap k;  // [.., Hkv, 64-row block, D] view of the ring or page pool
+    CUtensorMap v;
+};
+constexpr int kVerifyRows = 32;       // q_max * G rows per (request, kv head), padded
+constexpr int kVerifyBlock = 64;      // keys per pipeline stage (one GA page)
+constexpr int kVerifyChunkPages = 64; // pages per split of the GA context (4096 tokens)
+
+cudaError_t launch_verify_ring(const VerifyMaps &maps, const void *q, const int32_t *cu_q,
+                               const int32_t *seq_lens, const float *sink, void *o, int B, int Hq,
+                               int Hkv, int window, int R, int q_max, float scale,
+                               unsigned int *err, cudaStream_t s);
+cudaError_t launch_verify_paged(const VerifyMaps &maps, const void *q, const int32_t *cu_q,
+                                const int32_t *seq_lens, const int32_t *page_table, int max_pages,
+                                int num_pages, const float *sink, void *o, float *ws_o,
+                                float *ws_ml, int nsplit, int B, int Hq, int Hkv, int q_max,
+                                int max_ctx, float scale, unsigned int *err, cudaStream_t s);
+
+// Index dumps.
+cudaError_t launch_debug_prefill_visits(int32_t *visits, int mode, int T, int window, int G,
+                                        cudaStream_t s);
+cudaError_t launch_debug_verify_positions(int32_t *out, int kind, const int32_t *cu_q,
+                                          const int32_t *seq_lens, int B, int q_max, int window,
+                                          int R, int max_pages, int page_size, cudaStream_t s);
+
+}  // namespace attn

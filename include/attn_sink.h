@@ -1,0 +1,190 @@
+/*
+ * attn_sink.h -- C ABI of the B300 (sm_103a) sink-attention library.
+ *
+ * The operation: causal attention with a per-query-head learnable "sink"
+ * logit that joins the softmax denominator and carries no value, over either a
+ * sliding window of W keys (SWA layers, W = 128) or the full causal prefix
+ * (global-attention, GA, layers), in two modes: prefill over whole sequences,
+ * and the MTP self-speculative verify step that scores 1 real + up to 3 draft
+ * tokens per request against that request's KV cache.
+ *
+ * Sources (MiMo-V2-Flash):
+ *   [ARCH]   technical-report summary (fanfer.top, "MiMo-V2"), section
+ *            "MiMo-V2-Flash Model Architecture": 5 SWA layers then 1 GA layer
+ *            per hybrid block, sliding window W = 128.
+ *   [SINK]   same summary, section "Hybrid Sliding Window Attention
+ *            Architecture": learnable attention-sink bias in the gpt-oss style.
+ *            The formula that followed was lost from the page; this library
+ *            implements the reading "one extra softmax column per query head,
+ *            logit sigma_h compared unscaled with the scaled scores, zero value".
+ *   [KV]     release announcement (aihot.news, "小米开源 MiMo-V2-Flash"), section
+ *            "将效率推向极限": SWA keeps a fixed-size KV cache.
+ *   [MTP]    same announcement, figure "Multi-Token Prediction": the main model
+ *            verifies token i and drafts i+1..i+3 in one pass and keeps the
+ *            accepted prefix; summary section "MTP加速" (16K in / 1K out).
+ *
+ * Definition (all entry points):  for query position i of head h (kv head
+ * g = h / (Hq/Hkv)), visible keys j satisfy 0 <= j <= i and, for SWA,
+ * j >= i - W + 1.  With S_j = scale * <q_i, k_j>,
+ *     m = max(sigma_h, max_j S_j),  Z = e^(sigma_h - m) + sum_j e^(S_j - m),
+ *     o_i = sum_j e^(S_j - m) / Z * v_j,     lse_i = m + ln Z.
+ * sigma_h = +inf gives o_i = 0; sigma_h = -inf is plain softmax attention.
+ *
+ * Conventions:
+ *   - every pointer argument is a DEVICE pointer owned by the caller, except
+ *     where marked (host); the library never allocates and keeps no state
+ *     between calls other than a device error word;
+ *   - every call only enqueues work on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns without synchronising;
+ *   - tensors are dense row-major; q/k/v/o/cache pointers must be 16-byte
+ *     aligned (ATTN_ERR_INVALID_ARG otherwise);
+ *   - argument errors detectable on the host return ATTN_ERR_INVALID_ARG or
+ *     ATTN_ERR_UNSUPPORTED before anything is enqueued; attn_last_error()
+ *     then describes the problem;
+ *   - errors only the device can see (a page id outside the pool, a sequence
+ *     longer than the cache, q_len > q_max, a pipeline wait that timed out)
+ *     set bits in a device error word, the offending work is skipped (never a
+ *     trap), and attn_check_device_error() reports them.
+ */
+#ifndef ATTN_SINK_H
+#define ATTN_SINK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,   /* bad size, null or misaligned pointer        */
+    ATTN_ERR_UNSUPPORTED = 2,   /* well-formed but not implemented (e.g. D)    */
+    ATTN_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed           */
+    ATTN_ERR_DEVICE_FAULT = 4   /* the device error word is non-zero           */
+} attn_status_t;
+
+typedef enum attn_dtype {
+    ATTN_BF16 = 0,              /* bf16 I/O, fp32 accumulation, P rounded to bf16 before PV */
+    ATTN_F32 = 1                /* fp32 I/O and fp32 arithmetic on CUDA cores (no TF32)     */
+} attn_dtype_t;
+
+/* Bits of the device error word. */
+#define ATTN_DEVERR_PAGE_OOB     0x1u  /* page_table entry outside [0, num_pages)           */
+#define ATTN_DEVERR_CTX_OOB      0x2u  /* seq_len > max_ctx, > max_pages*page_size, or < q_len */
+#define ATTN_DEVERR_QLEN         0x4u  /* cu_q gives q_len > q_max                          */
+#define ATTN_DEVERR_WAIT_TIMEOUT 0x8u  /* an in-kernel pipeline wait exceeded its time limit  */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int attn_version(void);
+
+/* Thread-local description of the last host-side error ("" if none).  The
+ * string stays valid until the next call from the same thread. */
+const char *attn_last_error(void);
+
+/* Synchronises `stream`, reads and clears the device error word of the current
+ * device.  *bits_out (host, may be NULL) receives the ATTN_DEVERR_* bits.
+ * Returns ATTN_OK when the word was zero, ATTN_ERR_DEVICE_FAULT when not, and
+ * ATTN_ERR_CUDA when the synchronisation itself failed. */
+attn_status_t attn_check_device_error(void *stream, unsigned int *bits_out);
+
+/* ---------------------------------------------------------------- prefill ---
+ * Sliding-window prefill [ARCH][SINK].
+ *   q [B,T,Hq,D], k [B,T,Hkv,D], v [B,T,Hkv,D], o [B,T,Hq,D]   (dtype)
+ *   sink [Hq] fp32 logits;  lse [B,Hq,T] fp32 natural-log LSE, or NULL
+ *   window >= 1 (keys i-window+1..i);  scale > 0 (usually 1/sqrt(D))
+ * Supported: ATTN_BF16 with D = 128 and Hq/Hkv in {1,2,4,8} on the tensor-core
+ * path; ATTN_F32 with D in {64,128} on the fp32 CUDA-core path. */
+attn_status_t attn_swa_sink_prefill(const void *q, const void *k, const void *v, const float *sink,
+                                    void *o, float *lse, int B, int T, int Hq, int Hkv, int D,
+                                    int window, float scale, attn_dtype_t dtype, void *stream);
+
+/* Global (full causal) prefill [ARCH][SINK]; arguments as above without window. */
+attn_status_t attn_ga_sink_prefill(const void *q, const void *k, const void *v, const float *sink,
+                                   void *o, float *lse, int B, int T, int Hq, int Hkv, int D,
+                                   float scale, attn_dtype_t dtype, void *stream);
+
+/* ------------------------------------------------------------ KV caches ---
+ * SWA ring [KV][MTP]: ring_k, ring_v [B,Hkv,R,D] with R = ring_slots >=
+ * window + q_max - 1 (131 for W = 128, q_max = 4); position p of request b
+ * lives in slot p mod R.
+ * GA paged cache: k_pages, v_pages [num_pages,Hkv,page_size,D] (page_size =
+ * 64), page_table [B,max_pages] int32; position p of request b lives in page
+ * page_table[b, p / page_size] at offset p % page_size.
+ *
+ * Append: request b's q_len = cu_q[b+1]-cu_q[b] new tokens (k_new, v_new
+ * [cu_q[B],Hkv,D], rows cu_q[b]..) take positions seq_lens[b]-q_len ..
+ * seq_lens[b]-1 (seq_lens counts them).  cu_q [B+1], seq_lens [B] int32. */
+attn_status_t attn_swa_ring_append(const void *k_new, const void *v_new, const int32_t *cu_q,
+                                   const int32_t *seq_lens, void *ring_k, void *ring_v,
+                                   int B, int Hkv, int D, int ring_slots, int q_max,
+                                   attn_dtype_t dtype, void *stream);
+
+attn_status_t attn_ga_paged_append(const void *k_new, const void *v_new, const int32_t *cu_q,
+                                   const int32_t *seq_lens, void *k_pages, void *v_pages,
+                                   const int32_t *page_table, int max_pages, int num_pages,
+                                   int page_size, int B, int Hkv, int D, int q_max,
+                                   attn_dtype_t dtype, void *stream);
+
+/* ----------------------------------------------------------------- verify ---
+ * MTP verify [MTP]: request b scores its q_len = cu_q[b+1]-cu_q[b] <= q_max
+ * new tokens (positions seq_lens[b]-q_len .. seq_lens[b]-1, already appended)
+ * against its cache; draft t sees the history and drafts 0..t.
+ *   q, o [cu_q[B],Hq,D] (dtype);  sink [Hq] fp32;  q_max <= 4.
+ * Rejected drafts are rolled back by the caller lowering seq_lens; the next
+ * append overwrites their slots.  Supported: ATTN_BF16, D = 128,
+ * q_max * (Hq/Hkv) <= 32. */
+attn_status_t attn_swa_sink_verify(const void *q, const int32_t *cu_q, const void *ring_k,
+                                   const void *ring_v, const int32_t *seq_lens, const float *sink,
+                                   void *o, int B, int Hq, int Hkv, int D, int window,
+                                   int ring_slots, int q_max, float scale, attn_dtype_t dtype,
+                                   void *stream);
+
+/* Bytes of scratch that attn_ga_sink_verify needs for these sizes (split-KV
+ * partial results).  max_ctx bounds every seq_lens[b]. */
+size_t attn_ga_sink_verify_workspace(int B, int Hq, int Hkv, int D, int q_max, int max_ctx);
+
+/* GA verify over the paged cache, split over chunks of the context and merged
+ * by log-sum-exp; the sink enters once, in the merge.  `workspace` is a device
+ * buffer of at least attn_ga_sink_verify_workspace(...) bytes, 256-byte
+ * aligned, owned by the caller; its contents need no initialisation and are
+ * garbage afterwards.  Calls that share a workspace must not overlap. */
+attn_status_t attn_ga_sink_verify(const void *q, const int32_t *cu_q, const void *k_pages,
+                                  const void *v_pages, const int32_t *page_table, int max_pages,
+                                  int num_pages, int page_size, const int32_t *seq_lens,
+                                  const float *sink, void *o, void *workspace,
+                                  size_t workspace_bytes, int B, int Hq, int Hkv, int D,
+                                  int q_max, int max_ctx, float scale, attn_dtype_t dtype,
+                                  void *stream);
+
+/* ------------------------------------------------------------ index dumps ---
+ * Integer-exact views of the kernels' own index arithmetic (same device
+ * functions), for bit-exact tests against the definitions above.
+ *
+ * attn_debug_prefill_visits: counts, for every (query i, key j) of one head of
+ * a length-T sequence, how many times the prefill kernel's tile schedule and
+ * mask admit key j for query i.  visits [T,T] int32 (device).  mode 0 = the
+ * GA tiling (window <= 0 for full causal, else window-limited), mode 1 = the
+ * packed SWA tiling with G = Hq/Hkv heads per tile.  Correct kernels give 1
+ * exactly on visible pairs and 0 elsewhere. */
+attn_status_t attn_debug_prefill_visits(int32_t *visits, int mode, int T, int window, int G,
+                                        void *stream);
+
+/* attn_debug_verify_positions: for each request b, query t < q_max and cache
+ * slot s, the absolute position the verify kernel assigns to the key it reads
+ * there if that key is visible to query t, else -1.
+ *   kind 0 (ring):  out [B,q_max,ring_slots], slot = ring slot;
+ *   kind 1 (paged): out [B,q_max,max_pages*page_size], slot = page-table
+ *                   index * page_size + offset (the physical page read is
+ *                   page_table[b, slot / page_size]).
+ * cu_q, seq_lens as for verify; page_size is ignored for kind 0. */
+attn_status_t attn_debug_verify_positions(int32_t *out, int kind, const int32_t *cu_q,
+                                          const int32_t *seq_lens, int B, int q_max, int window,
+                                          int ring_slots, int max_pages, int page_size,
+                                          void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SINK_H */

@@ -1,0 +1,51 @@
+"""The C-ABI library loads on a CPU host and exports every declared entry
+point; argument errors are reported from the host before any CUDA work."""
+import ctypes
+import subprocess
+
+import pytest
+
+import global_attention_sinks_swa_b300 as A
+
+
+def test_every_declared_symbol_is_exported():
+    declared = A.declared_symbols()
+    assert len(declared) >= 12
+    out = subprocess.run(["nm", "-D", "--defined-only", A.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = [s for s in declared if s not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for s in declared:
+        assert getattr(A._lib, s) is not None
+
+
+def test_only_declared_symbols_are_public():
+    out = subprocess.run(["nm", "-D", "--defined-only", A.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    extra = sorted(s for s in exported if s.startswith("attn_") and s not in A.declared_symbols())
+    assert not extra, f"exported but not declared: {extra}"
+
+
+def test_version_and_error_string():
+    assert A.attn_version() >= 100
+    assert isinstance(A._lib.attn_last_error(), bytes)
+
+
+@pytest.mark.parametrize("fn,nargs", [("attn_swa_sink_prefill", 15), ("attn_ga_sink_prefill", 14)])
+def test_null_pointers_rejected_on_host(fn, nargs):
+    f = getattr(A._lib, fn)
+    args = [None] * 6 + [1, 16, 8, 1, 128] + ([128] if fn.startswith("attn_swa") else []) + \
+           [ctypes.c_float(0.1), 0, None]
+    assert len(args) == nargs
+    assert f(*args) == A.ATTN_ERR_INVALID_ARG
+    assert b"null" in A._lib.attn_last_error()
+
+
+def test_verify_workspace_size_formula():
+    # one split (context <= 4096) needs no scratch; otherwise 32 rows x (D + 2) floats per unit
+    assert A.attn_ga_sink_verify_workspace(64, 64, 8, 128, 4, 4096) == 0
+    n = A.attn_ga_sink_verify_workspace(64, 64, 8, 128, 4, 65536)
+    units = 64 * 8 * 16
+    assert n >= units * 32 * 130 * 4

@@ -1,0 +1,71 @@
+"""Failure reporting without a GPU fault: bad inputs that only the device can
+see set bits in the device error word (the offending work is skipped, no trap,
+no hang), and host-detectable errors return a status before any launch."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+A = pytest.importorskip("global_attention_sinks_swa_b300")
+pytestmark = pytest.mark.gpu
+
+Hq, Hkv, D = 64, 8, 128
+
+
+def _clear():
+    A.attn_check_device_error()
+
+
+def test_page_id_out_of_pool_sets_bit_and_context_survives():
+    _clear()
+    B, PAGE, num_pages = 2, 64, 8
+    page_table = torch.tensor([[0, 1, 2, 3], [4, 5, 99, 7]], dtype=torch.int32, device="cuda")
+    seq_lens = torch.tensor([150, 150], dtype=torch.int32, device="cuda")  # appends land in page index 2
+    cu_q = torch.tensor([0, 4, 8], dtype=torch.int32, device="cuda")
+    kp = synth.normal((num_pages, Hkv, PAGE, D), 1, device="cuda")
+    vp = synth.normal((num_pages, Hkv, PAGE, D), 2, device="cuda")
+    q = synth.normal((8, Hq, D), 3, device="cuda")
+    sink = synth.sink_logits(Hq, 4, device="cuda")
+    A.attn_ga_sink_verify(q, cu_q, kp, vp, page_table, seq_lens, sink, max_ctx=256)
+    assert A.attn_check_device_error() & A.DEVERR_PAGE_OOB
+    k_new = synth.normal((8, Hkv, D), 5, device="cuda")
+    A.attn_ga_paged_append(k_new, k_new.clone(), cu_q, seq_lens, kp, vp, page_table, q_max=4)
+    assert A.attn_check_device_error() & A.DEVERR_PAGE_OOB
+    # the context is still usable and the word was cleared
+    assert A.attn_check_device_error() == 0
+    assert torch.isfinite(torch.ones(4, device="cuda").sum())
+
+
+def test_qlen_above_qmax_and_short_context_set_bits():
+    _clear()
+    B, R = 2, 131
+    ring = synth.normal((B, Hkv, R, D), 1, device="cuda")
+    cu_q = torch.tensor([0, 4, 9], dtype=torch.int32, device="cuda")   # second request: 5 > q_max
+    seq_lens = torch.tensor([3, 100], dtype=torch.int32, device="cuda")  # first: L < q_len
+    q = synth.normal((9, Hq, D), 2, device="cuda")
+    sink = synth.sink_logits(Hq, 3, device="cuda")
+    A.attn_swa_sink_verify(q, cu_q, ring, ring.clone(), seq_lens, sink, window=128, q_max=4)
+    bits = A.attn_check_device_error()
+    assert bits & A.DEVERR_QLEN and bits & A.DEVERR_CTX_OOB
+
+
+def test_host_side_errors_return_status():
+    q = torch.zeros(1, 16, 8, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 16, 1, 128, dtype=torch.bfloat16, device="cuda")
+    sink = torch.zeros(8, device="cuda")
+    with pytest.raises(A.AttnError) as e:
+        A.attn_swa_sink_prefill(q, k, k, sink, window=0)
+    assert e.value.status == A.ATTN_ERR_INVALID_ARG
+    q64 = torch.zeros(1, 16, 8, 64, dtype=torch.bfloat16, device="cuda")
+    k64 = torch.zeros(1, 16, 1, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(A.AttnError) as e:
+        A.attn_ga_sink_prefill(q64, k64, k64, sink)
+    assert e.value.status == A.ATTN_ERR_UNSUPPORTED
+    ring = torch.zeros(1, 1, 100, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(A.AttnError) as e:   # ring smaller than window + q_max - 1
+        A.attn_swa_sink_verify(torch.zeros(4, 8, 128, dtype=torch.bfloat16, device="cuda"),
+                               torch.tensor([0, 4], dtype=torch.int32, device="cuda"), ring, ring,
+                               torch.tensor([10], dtype=torch.int32, device="cuda"), sink,
+                               window=128, q_max=4)
+    assert e.value.status == A.ATTN_ERR_INVALID_ARG
