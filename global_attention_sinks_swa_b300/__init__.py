@@ -50,6 +50,7 @@ _SIGS = {
     "attn_swa_sink_verify": ([_vp] * 7 + [_ci] * 7 + [_cf, _ci, _vp], _ci),
     "attn_ga_sink_verify_workspace": ([_ci] * 6, _sz),
     "attn_ga_sink_verify": ([_vp] * 5 + [_ci] * 3 + [_vp] * 4 + [_sz] + [_ci] * 6 + [_cf, _ci, _vp], _ci),
+    "attn_ga_sink_verify_noalloc": ([_vp] * 5 + [_ci] * 3 + [_vp] * 3 + [_ci] * 6 + [_cf, _ci, _vp], _ci),
     "attn_debug_prefill_visits": ([_vp] + [_ci] * 4 + [_vp], _ci),
     "attn_debug_verify_positions": ([_vp, _ci, _vp, _vp] + [_ci] * 6 + [_vp], _ci),
 }
@@ -223,6 +224,27 @@ def attn_ga_sink_verify(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, m
                                     _ptr(sink), _ptr(out), _ptr(workspace), ws_bytes, B, Hq, Hkv,
                                     D, int(q_max), int(max_ctx), scale, _dtype_code(q),
                                     _stream(stream)))
+    return out
+
+
+def attn_ga_sink_verify_noalloc(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink,
+                                max_ctx: int, q_max: int = 4, scale: float | None = None,
+                                out=None, stream=None):
+    """attn_ga_sink_verify for callers that cannot allocate device memory: the
+    split-KV scratch is the library's static 64 MiB device array (see the C
+    header for its limits; concurrent calls on one device race on it)."""
+    _cuda(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, out)
+    nq, Hq, D = q.shape
+    P, Hkv, page_size, _ = k_pages.shape
+    B, max_pages = page_table.shape
+    if out is None:
+        raise ValueError("pass a preallocated `out` (this entry point allocates nothing)")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(_lib.attn_ga_sink_verify_noalloc(_ptr(q), _ptr(cu_q), _ptr(k_pages), _ptr(v_pages),
+                                            _ptr(page_table), max_pages, P, page_size,
+                                            _ptr(seq_lens), _ptr(sink), _ptr(out), B, Hq, Hkv, D,
+                                            int(q_max), int(max_ctx), scale, _dtype_code(q),
+                                            _stream(stream)))
     return out
 
 

@@ -347,6 +347,60 @@ ATTN_EXPORT attn_status_t attn_ga_sink_verify(const void *q, const int32_t *cu_q
     return e == cudaSuccess ? ok() : cuda_fail(e, "ga verify launch");
 }
 
+// ---------------------------------------------- GA verify without allocation
+// Some callers cannot call cudaMalloc at all: code that runs inside a host
+// program which reserved all device memory up front in its own pool and
+// forbids later allocations, or a latency-critical decode loop that must
+// never risk the implicit device synchronisation and latency of an
+// allocation.  attn_ga_sink_verify_noalloc serves them: its split-KV partials
+// live in this file-scope device array instead of a caller workspace.  Every
+// GPU that loads the library holds the array until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_verify_scratch[kNoAllocScratchBytes];
+
+namespace {
+// Device address of g_verify_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device with cudaGetSymbolAddress (with that device current) and cached.
+void *noalloc_scratch() {
+    static void *addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress((void **)&ptr, g_verify_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+}  // namespace
+
+ATTN_EXPORT attn_status_t attn_ga_sink_verify_noalloc(
+    const void *q, const int32_t *cu_q, const void *k_pages, const void *v_pages,
+    const int32_t *page_table, int max_pages, int num_pages, int page_size,
+    const int32_t *seq_lens, const float *sink, void *o, int B, int Hq, int Hkv, int D, int q_max,
+    int max_ctx, float scale, attn_dtype_t dtype, void *stream) {
+    const size_t need = attn_ga_sink_verify_workspace(B, Hq, Hkv, D, q_max, max_ctx);
+    if (need > kNoAllocScratchBytes)
+        return fail(ATTN_ERR_UNSUPPORTED,
+                    "split-KV scratch of %zu bytes exceeds the %zu-byte static scratch of "
+                    "attn_ga_sink_verify_noalloc (lower B or max_ctx, or pass a workspace to "
+                    "attn_ga_sink_verify)",
+                    need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    if (need > 0) {
+        scratch = noalloc_scratch();
+        if (!scratch)
+            return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress of the static verify scratch failed");
+    }
+    return attn_ga_sink_verify(q, cu_q, k_pages, v_pages, page_table, max_pages, num_pages,
+                               page_size, seq_lens, sink, o, scratch,
+                               need > 0 ? kNoAllocScratchBytes : 0, B, Hq, Hkv, D, q_max, max_ctx,
+                               scale, dtype, stream);
+}
+
 ATTN_EXPORT attn_status_t attn_debug_prefill_visits(int32_t *visits, int mode, int T, int window,
                                                     int G, void *stream) {
     if (!visits || T < 0 || (mode != 0 && mode != 1))

@@ -157,6 +157,30 @@ attn_status_t attn_ga_sink_verify(const void *q, const int32_t *cu_q, const void
                                   int q_max, int max_ctx, float scale, attn_dtype_t dtype,
                                   void *stream);
 
+/* The same GA verify for callers that cannot allocate device memory (for
+ * example code inside a host program that reserved all device memory up front
+ * in its own pool and allows no later cudaMalloc, or a decode loop that must
+ * not pay an allocation's latency and possible device synchronisation).  It
+ * allocates nothing: the split-KV partials go to a 64 MiB file-scope device
+ * array inside the library, which every GPU that loads the library holds until
+ * the process exits.  The pages have no counterpart to this entry point.
+ *   - Arguments and results as attn_ga_sink_verify, without the workspace.
+ *   - Sizes whose scratch (attn_ga_sink_verify_workspace) exceeds 64 MiB are
+ *     rejected with ATTN_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     every value a call reads is written earlier in the same call, so nothing
+ *     needs clearing.  Calls that overlap on the GPU (other streams, other
+ *     host threads on the same device) race on the array. */
+attn_status_t attn_ga_sink_verify_noalloc(const void *q, const int32_t *cu_q, const void *k_pages,
+                                          const void *v_pages, const int32_t *page_table,
+                                          int max_pages, int num_pages, int page_size,
+                                          const int32_t *seq_lens, const float *sink, void *o,
+                                          int B, int Hq, int Hkv, int D, int q_max, int max_ctx,
+                                          float scale, attn_dtype_t dtype, void *stream);
+
 /* ------------------------------------------------------------ index dumps ---
  * Integer-exact views of the kernels' own index arithmetic (same device
  * functions), for bit-exact tests against the definitions above.
