@@ -90,60 +90,112 @@ def ncu_traffic(kernel_file: str, name: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """SM clock and throttle reasons sampled during a timed region (read-only
+    queries).  NVML is polled every ~2 ms in a thread when the `pynvml`
+    module is present; otherwise `nvidia-smi -lms 20` runs for the region and
+    the sampler waits for its first line before the region starts."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    NVML_REASONS = ("nvmlClocksEventReasonHwSlowdown", "nvmlClocksEventReasonHwThermalSlowdown",
+                    "nvmlClocksEventReasonSwThermalSlowdown", "nvmlClocksEventReasonSwPowerCap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+        self.samples = []      # (sm_mhz, set of active reason names)
+        self.sm_max = None
+        self.source = "unavailable"
+        self.error = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+
+    # -- NVML
+    def _nvml_poll(self):
+        p = self._nvml
+        while not self._stop.is_set():
+            self._nvml_once()
+            time.sleep(0.002)
+
+    def _nvml_once(self):
+        p = self._nvml
+        try:
+            mhz = float(p.nvmlDeviceGetClockInfo(self._h, p.NVML_CLOCK_SM))
+            mask = int(p.nvmlDeviceGetCurrentClocksEventReasons(self._h))
+        except Exception:  # noqa: BLE001
+            return
+        self.samples.append((mhz, {n for n, a in zip(self.NAMES, self.NVML_REASONS)
+                                   if mask & getattr(p, a, 0)}))
+
+    # -- nvidia-smi
+    def _smi_read(self):
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                mhz, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            self.sm_max = mx
+            self.samples.append((mhz, {n for n, v in zip(self.NAMES, parts[2:6])
+                                       if v.lower() == "active"}))
+            self._first.set()
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
+            import pynvml
+            pynvml.nvmlInit()
+            self._nvml = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.gpu)
+            self.sm_max = float(pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM))
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._nvml_poll, daemon=True)
+            self._thread.start()
+            return self
+        except Exception as e:  # noqa: BLE001
+            self.error = f"nvml: {type(e).__name__}: {e}"
+        try:
+            import subprocess
+            self._first = threading.Event()
+            self._proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except Exception:
-            self.proc = None
+            self._thread = threading.Thread(target=self._smi_read, daemon=True)
+            self._thread.start()
+            self._first.wait(timeout=3.0)
+            self.source = "nvidia-smi"
+        except Exception as e:  # noqa: BLE001
+            self.error = (self.error or "") + f"; nvidia-smi: {type(e).__name__}: {e}"
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            time.sleep(0.03)   # one more nvidia-smi line after the region
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+                self._proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+        if self.source == "nvml" and not self.samples:
+            self._nvml_once()
+        return False
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": None, "sm_max_mhz": self.sm_max, "reasons": [], "samples": len(self.samples),
+               "source": self.source}
+        if self.samples:
+            out["sm_mhz"] = statistics.median(m for m, _ in self.samples)
+            out["reasons"] = sorted(set().union(*(r for _, r in self.samples)))
+        if self.error:
+            out["note"] = self.error
+        return out
 
 
 # ----------------------------------------------------------- distributed
@@ -172,22 +224,33 @@ def barrier(world: int):
 
 
 # ------------------------------------------------------------ GPU timing
-def time_region(fn, steps: int, world: int, stream):
-    """CUDA-event time of `steps` calls of fn on `stream`, barrier + sync on both sides."""
+class _NoSampler:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+def time_region(fn, steps: int, world: int, stream, sampler=None):
+    """CUDA-event time of `steps` calls of fn on `stream`, barrier + sync on
+    both sides; `sampler` (a ClockSampler) runs only around the region."""
     import torch
     barrier(world)
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(steps):
-        fn(i)
-    stop.record(stream)
-    torch.cuda.synchronize()
+    with (sampler or _NoSampler()):
+        start.record(stream)
+        for i in range(steps):
+            fn(i)
+        stop.record(stream)
+        torch.cuda.synchronize()
     barrier(world)
     return start.elapsed_time(stop) / steps
 
 
-def bench_prefill(A, synth, kind: str, steps: int, warmup: int, world: int, stream, seed: int):
+def bench_prefill(A, synth, kind: str, steps: int, warmup: int, world: int, stream, seed: int,
+                  sampler=None):
     import torch
     sets = []
     for s in range(2):   # two rotating input sets; each set (1.2 GB) exceeds L2
@@ -205,7 +268,7 @@ def bench_prefill(A, synth, kind: str, steps: int, warmup: int, world: int, stre
     with torch.cuda.stream(stream):
         for i in range(warmup):
             step(i)
-        ms = time_region(step, steps, world, stream)
+        ms = time_region(step, steps, world, stream, sampler)
     if A.attn_check_device_error(stream) != 0:
         raise RuntimeError(f"{kind} prefill reported a device error")
     return ms, prefill_flop(T, window)
@@ -343,10 +406,13 @@ def cpu_baseline(seconds_target: float = 15.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-parts", action="store_true", help="headline only")
+    ap.add_argument("--profile", default="",
+                    help="comma list of swa,ga,verify_ga,verify_swa: run only these kernels "
+                         "(warmup + steps), no JSON line; for ncu captures")
     args = ap.parse_args()
     world, rank, local = dist_env()
     warmup = max(3, args.warmup)
@@ -366,8 +432,11 @@ def main():
     stream = torch.cuda.Stream()
     hbm, tf_burst, tf_sus, peak_src = load_peaks()
 
-    with ClockSampler(local) as clocks:
-        ms, flop = bench_prefill(A, synth, "swa", args.steps, warmup, world, stream, 1002 + 10 * rank)
+    if args.profile:
+        return run_profile(A, synth, args, warmup, stream)
+    clocks = ClockSampler(local)
+    ms, flop = bench_prefill(A, synth, "swa", args.steps, warmup, world, stream, 1002 + 10 * rank,
+                             clocks)
     ms_max = reduce_max(ms, world, torch.device("cuda", local))
     value = world * flop / (ms_max * 1e-3) / 1e12
     achieved = prefill_min_bytes() / (ms * 1e-3) / 1e9
@@ -447,6 +516,22 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_profile(A, synth, args, warmup, stream):
+    """Only the named kernels, for profiler captures (sizes: the headline and
+    GA prefill at full size, 1.2 GB each; GA verify on 16 requests ~ 2.3 GB)."""
+    for name in args.profile.split(","):
+        if name in ("swa", "ga"):
+            bench_prefill(A, synth, name, args.steps, warmup, 1, stream, 1002)
+        elif name == "verify_ga":
+            ctx = synth.context_lengths(16, 4096, 65536, 1004)
+            bench_verify_ga(A, ctx, np.full(16, QMAX, np.int32), args.steps, warmup, 1, stream, 1004)
+        elif name == "verify_swa":
+            bench_verify_swa(A, 64, args.steps, warmup, 1, stream, 2004)
+        else:
+            raise SystemExit(f"unknown profile target {name}")
+    print(json.dumps({"profile": args.profile, "ok": True}), flush=True)
 
 
 def run_reference(args, world, rank, warmup):

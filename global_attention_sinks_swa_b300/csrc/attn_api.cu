@@ -129,6 +129,7 @@ attn_status_t prefill_common(const void *q, const void *k, const void *v, const 
     if (B == 0 || T == 0) return ok();
     const int G = Hq / Hkv;
     attn::PrefillMaps maps;
+    maps.out = o;
     const bool packed = swa && attn::prefill_swa_tc_supported(G, window);
     bool good;
     if (packed) {

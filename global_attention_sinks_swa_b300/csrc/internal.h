@@ -19,6 +19,7 @@ struct PrefillMaps {
     CUtensorMap k;  // key tile
     CUtensorMap v;  // value tile
     CUtensorMap o;  // output store
+    void *out;      // output base pointer (kernels that store O without TMA)
 };
 
 // tcgen05 GA-tiled prefill (full causal, or window-limited when window > 0).

@@ -298,15 +298,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             float x[128];
             tmem_load_row<128>(tS, x);
-            const bool masked = ga_tile_needs_mask(qs, j, window);
-            float mx = -INFINITY;
+            // row max of the raw scores (scale > 0 commutes with max), four
+            // independent partial maxima; masked entries become -inf
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (ga_tile_needs_mask(qs, j, window)) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                float v = x[c] * sl2;
-                if (masked && !key_visible(qpos, j * 128 + c, window)) v = -INFINITY;
-                x[c] = v;
-                mx = fmaxf(mx, v);
+                for (int c = 0; c < 128; ++c) {
+                    if (!key_visible(qpos, j * 128 + c, window)) x[c] = -INFINITY;
+                    m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
             }
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
             // lazy max: raise m only when the tile max exceeds it by > 2^8
             const bool grow = mx > m + kRescaleLog2;
             const bool any_grow = __any_sync(0xffffffffu, grow);
@@ -315,20 +320,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
             m = mn;
             const float mb = (m == -INFINITY) ? 0.f : m;
-            float rs = 0.f;
+            float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {  // P = 2^(x - m) as bf16 over the S columns
+            for (int c = 0; c < 4; ++c) {  // P = 2^(s*scale*log2e - m) as bf16 over the S columns
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ptx::exp2_approx(x[32 * c + 2 * i] - mb);
-                    const float p1 = ptx::exp2_approx(x[32 * c + 2 * i + 1] - mb);
-                    rs += p0 + p1;
+                    const float p0 = ptx::exp2_approx(fmaf(x[32 * c + 2 * i], sl2, -mb));
+                    const float p1 = ptx::exp2_approx(fmaf(x[32 * c + 2 * i + 1], sl2, -mb));
+                    r4[(2 * i) & 3] += p0;
+                    r4[(2 * i + 1) & 3] += p1;
                     pk[i] = ptx::pack_bf16x2(p0, p1);
                 }
                 ptx::tmem_st16(tS + 16 * c, pk);
             }
-            l += rs;
+            l += (r4[0] + r4[1]) + (r4[2] + r4[3]);
             if (any_grow && nt > 0) {  // rescale the O accumulator after the previous PV
                 if (!ptx::mbar_wait_warp(&sm.o_full[t], (nt - 1) & 1)) { ok = false; break; }
                 ptx::tc_fence_after();
@@ -381,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // =========================================================== packed SWA kernel
 namespace swa {
 
-constexpr int kThreads = 320;  // WG0 (slot 0), WG1 (slot 1), warp 8 TMA, warp 9 MMA
+constexpr int kThreads = 352;  // WG0 (slot 0), WG1 (slot 1), warp 8 Q/K TMA, warp 9 MMA, warp 10 V TMA
 constexpr int kN = 144;        // keys per tile (G = 8, W <= 129)
 constexpr int kQBytes = 128 * kHalfRowBytes;   // 16 KB per D half
 constexpr int kKBytes = kN * kHalfRowBytes;    // 18 KB per D half
@@ -394,8 +400,8 @@ static_assert(kOCol + 128 <= 256, "slot TMEM budget");
 struct __align__(1024) Smem {
     uint8_t q[2][2][kQBytes];  // [slot][D half]
     uint8_t k[2][2][kKBytes];
-    uint8_t v[2][2][kKBytes];  // V, then the O tile staged for the TMA store
-    uint64_t qk_full[2], v_full[2], s_full[2], p_full[2], o_full[2], tmem_free[2], v_free[2];
+    uint8_t v[2][2][kKBytes];
+    uint64_t qk_full[2], v_full[2], s_full[2], p_full[2], o_full[2], tmem_free[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -411,13 +417,26 @@ ATTN_DEV TileCoord tile_coord(int u, int nblk, int Hkv, int TT) {
     return c;
 }
 
+// Scaled max over NC columns starting at column c0 of this row, restricted to
+// the visible range [c_lo, c_hi], with four independent partial maxima.
+template <int NC>
+ATTN_DEV float chunk_max(const float (&x)[NC], int c0, int c_lo, int c_hi, float sl2) {
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+        const int c = c0 + i;
+        const bool vis = static_cast<unsigned>(c - c_lo) <= static_cast<unsigned>(c_hi - c_lo);
+        m4[i & 3] = fmaxf(m4[i & 3], vis ? x[i] : -INFINITY);
+    }
+    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_swa_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv,
-                       const __grid_constant__ CUtensorMap tmo, const float *__restrict__ sink,
-                       float *__restrict__ lse, int B, int T, int Hq, int Hkv, int window,
-                       float scale, unsigned *err) {
+                       const __grid_constant__ CUtensorMap tmv, __nv_bfloat16 *__restrict__ out,
+                       const float *__restrict__ sink, float *__restrict__ lse, int B, int T,
+                       int Hq, int Hkv, int window, float scale, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
@@ -437,7 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&sm.p_full[s], 128);
             ptx::mbar_init(&sm.o_full[s], 1);
             ptx::mbar_init(&sm.tmem_free[s], 128);
-            ptx::mbar_init(&sm.v_free[s], 1);
         }
         sm.abort = ptx::prior_timeout(err) ? 1 : 0;
         ptx::fence_mbar_init();
@@ -452,33 +470,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     const bool skip = sm.abort != 0;  // an earlier launch timed out: do nothing
 
-    if (warp == 8) {
-        // ------------------------------------------------------------ TMA
+    if (warp == 8 || warp == 10) {
+        // ------------------------------------------ TMA producers (Q/K and V)
+        // Q and K of a slot are free once its S MMA completed; V once its PV
+        // MMA completed.  Two producer warps keep the two streams independent.
         if (lane == 0 && !skip) {
-            ptx::prefetch_tmap(&tmq);
-            ptx::prefetch_tmap(&tmk);
-            ptx::prefetch_tmap(&tmv);
-            for (int k = 0; k < ncta; ++k) {
+            bool ok = true;
+            const bool qk = (warp == 8);
+            if (qk) {
+                ptx::prefetch_tmap(&tmq);
+                ptx::prefetch_tmap(&tmk);
+            } else {
+                ptx::prefetch_tmap(&tmv);
+            }
+            for (int k = 0; ok && k < ncta; ++k) {
                 const int s = k & 1, u = k >> 1;
                 const TileCoord c = tile_coord(tile_of(k), nblk, Hkv, TT);
                 const int key0 = swa_pack_key0(c.i0, G, window);
-                // Q and K buffers free once S of this slot's previous tile completed
-                if (u > 0 && !ptx::mbar_wait(&sm.s_full[s], (u - 1) & 1)) goto fail8;
-                ptx::mbar_arrive_expect_tx(&sm.qk_full[s], 2 * kQBytes + 2 * kKBytes);
-                for (int hf = 0; hf < 2; ++hf) {
-                    ptx::tma_load_4d(sm.q[s][hf], &tmq, hf * 64, c.g * G, c.i0, c.b, &sm.qk_full[s]);
-                    ptx::tma_load_4d(sm.k[s][hf], &tmk, hf * 64, c.g, key0, c.b, &sm.qk_full[s]);
+                if (qk) {
+                    if (u > 0 && !ptx::mbar_wait(&sm.s_full[s], (u - 1) & 1)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(&sm.qk_full[s], 2 * kQBytes + 2 * kKBytes);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        ptx::tma_load_4d(sm.q[s][hf], &tmq, hf * 64, c.g * G, c.i0, c.b, &sm.qk_full[s]);
+                        ptx::tma_load_4d(sm.k[s][hf], &tmk, hf * 64, c.g, key0, c.b, &sm.qk_full[s]);
+                    }
+                } else {
+                    if (u > 0 && !ptx::mbar_wait(&sm.o_full[s], (u - 1) & 1)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(&sm.v_full[s], 2 * kKBytes);
+                    for (int hf = 0; hf < 2; ++hf)
+                        ptx::tma_load_4d(sm.v[s][hf], &tmv, hf * 64, c.g, key0, c.b, &sm.v_full[s]);
                 }
-                // V buffer free once the previous O tile left it
-                if (u > 0 && !ptx::mbar_wait(&sm.v_free[s], (u - 1) & 1)) goto fail8;
-                ptx::mbar_arrive_expect_tx(&sm.v_full[s], 2 * kKBytes);
-                for (int hf = 0; hf < 2; ++hf)
-                    ptx::tma_load_4d(sm.v[s][hf], &tmv, hf * 64, c.g, key0, c.b, &sm.v_full[s]);
             }
-            goto done8;
-        fail8:
-            atomicOr(err, kErrWait);
-        done8:;
+            if (!ok) atomicOr(err, kErrWait);
         }
         __syncwarp();
     } else if (warp == 9) {
@@ -516,8 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (!skip) {
         // ------------------------------------------------ softmax warpgroups
-        // Failure decisions are taken jointly by the warpgroup at its named
-        // barrier (bar.red.or), so an error unwinds without a hang.
+        // One thread per row (TMEM lane).  Failure decisions are warp-uniform
+        // and there is no barrier inside the loop, so an error never splits a
+        // warpgroup at a barrier.
         const int s = warp >> 2;
         const int row = threadIdx.x & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -529,64 +553,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileCoord c = tile_coord(tile_of(k), nblk, Hkv, TT);
             const int key0 = swa_pack_key0(c.i0, G, window);
             const int qpos = c.i0 + t_in, h = c.g * G + hh;
+            // visible key columns of this row: [c_lo, c_hi]
+            const int c_hi = qpos - key0;
+            const int c_lo = max(qpos - window + 1, 0) - key0;
             const float sig = sink[h];
-            bool okw = ptx::mbar_wait_warp(&sm.s_full[s], u & 1);
-            bool sink_all = false;
-            float mb = 0.f, l = 0.f;
-            if (okw) {
-                ptx::tc_fence_after();
-                // pass 1: row max over the visible scores, seeded with the sink logit
-                float m = sig * kLog2e;
-#pragma unroll
-                for (int c = 0; c < kN / 48; ++c) {
-                    float x[48];
-                    tmem_load_row<48>(tS + 48 * c, x);
-#pragma unroll
-                    for (int i = 0; i < 48; ++i)
-                        if (key_visible(qpos, key0 + 48 * c + i, window)) m = fmaxf(m, x[i] * sl2);
-                }
-                mb = (m == -INFINITY || m == INFINITY) ? 0.f : m;
-                // the sink's own term starts the sum
-                l = (isinf(sig) && sig < 0.f) ? 0.f : ptx::exp2_approx(sig * kLog2e - mb);
-                sink_all = isinf(sig) && sig > 0.f;
-                // pass 2: P = 2^(s - m) as bf16 over the S columns (P column c/2 <= S column c)
-#pragma unroll
-                for (int c = 0; c < kN / 48; ++c) {
-                    float x[48];
-                    tmem_load_row<48>(tS + 48 * c, x);
-#pragma unroll
-                    for (int i = 0; i < 48; ++i) {
-                        const bool vis = key_visible(qpos, key0 + 48 * c + i, window) && !sink_all;
-                        x[i] = vis ? ptx::exp2_approx(fmaf(x[i], sl2, -mb)) : 0.f;
-                        l += x[i];
-                    }
-                    tmem_store_p<48>(tS + 24 * c, x);
-                }
-                ptx::tmem_st_wait();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(&sm.p_full[s]);
-                okw = ptx::mbar_wait_warp(&sm.o_full[s], u & 1);
-            }
-            if (okw) {
-                ptx::tc_fence_after();
-                const float inv = sink_all ? 0.f : 1.f / l;
-                store_o_row_smem(tO, inv, sm.v[s][0], sm.v[s][1], row);
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(&sm.tmem_free[s]);
-                ptx::fence_proxy_async_smem();
-            }
-            if (ptx::named_bar_or(1 + s, 128, !okw)) {
-                if (row == 0) atomicOr(err, kErrWait);
+            if (!ptx::mbar_wait_warp(&sm.s_full[s], u & 1)) {
+                if (lane == 0) atomicOr(err, kErrWait);
                 break;
             }
-            if (row == 0) {
-                for (int hf = 0; hf < 2; ++hf)
-                    ptx::tma_store_4d(&tmo, sm.v[s][hf], hf * 64, c.g * G, c.i0, c.b);
-                ptx::bulk_commit();
-                ptx::bulk_wait_read0();
-                ptx::mbar_arrive(&sm.v_free[s]);
+            ptx::tc_fence_after();
+            // pass 1: row max over the visible scores, seeded with the sink logit
+            float m = sig * kLog2e;
+#pragma unroll
+            for (int cc = 0; cc < kN / 48; ++cc) {
+                float x[48];
+                tmem_load_row<48>(tS + 48 * cc, x);
+                m = fmaxf(m, chunk_max<48>(x, 48 * cc, c_lo, c_hi, sl2));
             }
-            if (lse && qpos < T)
+            const bool sink_all = isinf(sig) && sig > 0.f;
+            const float mb = (m == -INFINITY || sink_all) ? 0.f : m;
+            // pass 2: P = 2^(s*scale*log2e - m) as bf16 over the S columns
+            // (P column c/2 <= S column c, already read); four partial sums
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int cc = 0; cc < kN / 48; ++cc) {
+                float x[48];
+                tmem_load_row<48>(tS + 48 * cc, x);
+#pragma unroll
+                for (int i = 0; i < 48; ++i) {
+                    const int col = 48 * cc + i;
+                    const bool vis = static_cast<unsigned>(col - c_lo) <=
+                                     static_cast<unsigned>(c_hi - c_lo);
+                    x[i] = (vis && !sink_all) ? ptx::exp2_approx(fmaf(x[i], sl2, -mb)) : 0.f;
+                    l4[i & 3] += x[i];
+                }
+                tmem_store_p<48>(tS + 24 * cc, x);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&sm.p_full[s]);
+            // the sink's own term joins the sum
+            float l = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            if (!(isinf(sig) && sig < 0.f) && !sink_all) l += ptx::exp2_approx(sig * kLog2e - mb);
+
+            if (!ptx::mbar_wait_warp(&sm.o_full[s], u & 1)) {
+                if (lane == 0) atomicOr(err, kErrWait);
+                break;
+            }
+            ptx::tc_fence_after();
+            // epilogue: O row from TMEM, normalised, straight to global memory
+            const float inv = sink_all ? 0.f : 1.f / l;
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                out + ((static_cast<long>(c.b) * T + min(qpos, T - 1)) * Hq + h) * 128);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {  // 32 columns at a time: load, pack, store
+                uint32_t r[32];
+                ptx::tmem_ld32(tO + cc * 32, r);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                reg_dep(r);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv,
+                                             __uint_as_float(r[2 * i + 1]) * inv);
+                if (qpos < T) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[cc * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&sm.tmem_free[s]);  // S/O columns of this slot may be reused
+            if (qpos < T && lse)
                 lse[(static_cast<long>(c.b) * Hq + h) * T + qpos] =
                     sink_all ? INFINITY : (mb + log2f(l)) * kLn2;
         }
@@ -646,9 +684,9 @@ cudaError_t launch_prefill_swa_tc(const PrefillMaps &maps, const float *sink, fl
     const int G = Hq / Hkv, TT = swa_pack_tokens(G);
     const long ntiles = static_cast<long>((T + TT - 1) / TT) * Hkv * B;
     const int grid = static_cast<int>(ntiles < num_sms() ? ntiles : num_sms());
-    swa::prefill_swa_kernel<<<grid, swa::kThreads, smem, s>>>(maps.q, maps.k, maps.v, maps.o, sink,
-                                                              lse, B, T, Hq, Hkv, window, scale,
-                                                              err);
+    swa::prefill_swa_kernel<<<grid, swa::kThreads, smem, s>>>(
+        maps.q, maps.k, maps.v, static_cast<__nv_bfloat16 *>(maps.out), sink, lse, B, T, Hq, Hkv,
+        window, scale, err);
     return cudaGetLastError();
 }
 
