@@ -52,6 +52,7 @@ _SIGS = {
     "attn_ga_sink_verify": ([_vp] * 5 + [_ci] * 3 + [_vp] * 4 + [_sz] + [_ci] * 6 + [_cf, _ci, _vp], _ci),
     "attn_ga_sink_verify_noalloc": ([_vp] * 5 + [_ci] * 3 + [_vp] * 3 + [_ci] * 6 + [_cf, _ci, _vp], _ci),
     "attn_debug_prefill_visits": ([_vp] + [_ci] * 4 + [_vp], _ci),
+    "attn_debug_swa_stream_visits": ([_vp] + [_ci] * 5 + [_vp], _ci),
     "attn_debug_verify_positions": ([_vp, _ci, _vp, _vp] + [_ci] * 6 + [_vp], _ci),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -254,6 +255,16 @@ def attn_debug_prefill_visits(T: int, window: int, mode: int, G: int = 8, device
     visits = torch.empty(T, T, dtype=torch.int32, device=device)
     _check(_lib.attn_debug_prefill_visits(_ptr(visits), int(mode), T, int(window), int(G),
                                           _stream(stream)))
+    return visits
+
+
+def attn_debug_swa_stream_visits(B: int, T: int, Hkv: int, window: int = 128, grid: int = 0,
+                                 device="cuda", stream=None):
+    """[B*Hkv,T,T+1] int32 visit counts of the streaming SWA prefill schedule
+    (column T counts admitted keys outside [0,T)); grid 0 = the kernel's own."""
+    visits = torch.zeros(B * Hkv, T, T + 1, dtype=torch.int32, device=device)
+    _check(_lib.attn_debug_swa_stream_visits(_ptr(visits), B, T, Hkv, int(window), int(grid),
+                                             _stream(stream)))
     return visits
 
 

@@ -132,11 +132,11 @@ attn_status_t prefill_common(const void *q, const void *k, const void *v, const 
     maps.out = o;
     const bool packed = swa && attn::prefill_swa_tc_supported(G, window);
     bool good;
-    if (packed) {
-        const uint32_t TT = static_cast<uint32_t>(attn::swa_pack_tokens(G));
-        const uint32_t N = static_cast<uint32_t>(attn::swa_pack_keys(G, window));
-        good = map_bthd(&maps.q, q, B, T, Hq, G, TT) && map_bthd(&maps.k, k, B, T, Hkv, 1, N) &&
-               map_bthd(&maps.v, v, B, T, Hkv, 1, N) && map_bthd(&maps.o, o, B, T, Hq, G, TT);
+    if (packed) {  // Q tiles of 16 tokens x 8 heads; K/V in 16-key ring blocks
+        const uint32_t TT = static_cast<uint32_t>(attn::kSwaTokens);
+        const uint32_t NB = static_cast<uint32_t>(attn::kSwaBlockKeys);
+        good = map_bthd(&maps.q, q, B, T, Hq, G, TT) && map_bthd(&maps.k, k, B, T, Hkv, 1, NB) &&
+               map_bthd(&maps.v, v, B, T, Hkv, 1, NB);
     } else {
         good = map_bthd(&maps.q, q, B, T, Hq, 1, 128) && map_bthd(&maps.k, k, B, T, Hkv, 1, 128) &&
                map_bthd(&maps.v, v, B, T, Hkv, 1, 128) && map_bthd(&maps.o, o, B, T, Hq, 1, 128);
@@ -411,6 +411,18 @@ ATTN_EXPORT attn_status_t attn_debug_prefill_visits(int32_t *visits, int mode, i
         return fail(ATTN_ERR_UNSUPPORTED, "packed SWA tiling needs 128 % G == 0 and a window that fits");
     cudaError_t e = attn::launch_debug_prefill_visits(visits, mode, T, window, G, as_stream(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "debug prefill visits");
+}
+
+ATTN_EXPORT attn_status_t attn_debug_swa_stream_visits(int32_t *visits, int B, int T, int Hkv,
+                                                       int window, int grid, void *stream) {
+    if (!visits || B < 0 || T < 0 || Hkv < 1 || grid < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "bad arguments");
+    if (!attn::prefill_swa_tc_supported(attn::kSwaHeads, window))
+        return fail(ATTN_ERR_UNSUPPORTED, "the streaming SWA kernel needs a window in [114, 129]");
+    if (grid == 0 && B > 0 && T > 0) grid = attn::prefill_swa_grid(B, T, Hkv);
+    cudaError_t e = attn::launch_debug_swa_stream_visits(visits, B, T, Hkv, window, grid,
+                                                         as_stream(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "debug swa stream visits");
 }
 
 ATTN_EXPORT attn_status_t attn_debug_verify_positions(int32_t *out, int kind, const int32_t *cu_q,

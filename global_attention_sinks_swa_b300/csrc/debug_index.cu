@@ -40,6 +40,47 @@ __global__ void visits_swa_kernel(int32_t *visits, int T, int window, int G) {
     }
 }
 
+// Streaming SWA schedule: one thread per CTA of the kernel's grid replays
+// that CTA's run of tiles, the ring bookkeeping (which key block each ring
+// slot holds when a tile reads it) and the admitted columns, for query head 0
+// of each kv group.  visits [B*Hkv, T, T+1]; column T counts admitted keys
+// outside [0, T).
+__global__ void swa_stream_visits_kernel(int32_t *visits, int B, int T, int Hkv, int window,
+                                         int grid) {
+    const int cta = blockIdx.x * blockDim.x + threadIdx.x;
+    if (cta >= grid) return;
+    const int nblk = (T + kSwaTokens - 1) / kSwaTokens;
+    const int ntiles = nblk * Hkv * B;
+    int u0, u1;
+    swa_stream_range(cta, grid, ntiles, &u0, &u1);
+    SwaRingCursor cur;
+    int slot_key[kSwaRingBlocks];
+    for (int s = 0; s < kSwaRingBlocks; ++s) slot_key[s] = -(1 << 30);
+    for (int u = u0; u < u1; ++u) {
+        const int bg = u / nblk, i0 = (u - bg * nblk) * kSwaTokens;
+        const int key0 = i0 + kSwaTokens - kSwaKeys;
+        swa_ring_step(cur, bg, kSwaTileBlocks);
+        for (int s = cur.first_new; s < cur.first_new + cur.n_new; ++s)
+            slot_key[s % kSwaRingBlocks] = key0 + kSwaBlockKeys * (s - cur.base);
+        const bool interior = key0 >= 0;
+        for (int t = 0; t < kSwaTokens; ++t) {
+            const int qpos = i0 + t;
+            if (qpos >= T) break;
+            int c_lo, c_hi;
+            swa_row_cols(qpos, key0, window, &c_lo, &c_hi);
+            int32_t *row = visits + (static_cast<long>(bg) * T + qpos) * (T + 1);
+            for (int j = 0; j < kSwaTileBlocks; ++j) {
+                const int kb = slot_key[(cur.base + j) % kSwaRingBlocks];
+                for (int cc = 0; cc < kSwaBlockKeys; ++cc) {
+                    if (!swa_col_admitted(j * kSwaBlockKeys + cc, c_lo, c_hi, interior)) continue;
+                    const int key = kb + cc;
+                    atomicAdd(&row[(key >= 0 && key < T) ? key : T], 1);
+                }
+            }
+        }
+    }
+}
+
 __global__ void verify_positions_kernel(int32_t *out, int kind, const int32_t *cu_q,
                                         const int32_t *seq_lens, int q_max, int window, int R,
                                         int max_pages, int page_size) {
@@ -83,6 +124,16 @@ cudaError_t launch_debug_prefill_visits(int32_t *visits, int mode, int T, int wi
         visits_ga_kernel<<<blocks, 128, 0, s>>>(visits, T, window);
     else
         visits_swa_kernel<<<blocks, 128, 0, s>>>(visits, T, window, G);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_swa_stream_visits(int32_t *visits, int B, int T, int Hkv, int window,
+                                           int grid, cudaStream_t s) {
+    if (B == 0 || T == 0 || grid == 0) return cudaSuccess;
+    cudaError_t e = cudaMemsetAsync(
+        visits, 0, sizeof(int32_t) * static_cast<size_t>(B) * Hkv * T * (T + 1), s);
+    if (e != cudaSuccess) return e;
+    swa_stream_visits_kernel<<<(grid + 127) / 128, 128, 0, s>>>(visits, B, T, Hkv, window, grid);
     return cudaGetLastError();
 }
 

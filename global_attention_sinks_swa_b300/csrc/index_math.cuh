@@ -70,6 +70,72 @@ ATTN_HD int swa_pack_key0(int i0, int G, int window) {
     return i0 + swa_pack_tokens(G) - swa_pack_keys(G, window);
 }
 
+// ---- streaming SWA prefill (G = 8, 16 tokens x 8 heads per tile, N = 144):
+// a CTA walks a contiguous run of tiles in the order u = (b*Hkv + g)*nblk + blk
+// and keeps the keys of the current window in a ring of 16-key blocks in
+// shared memory, so each tile loads one new K/V block (nine after a change of
+// (b, g) or at the start of the run).
+constexpr int kSwaBlockKeys = 16;                 // keys per ring block
+constexpr int kSwaHeads = 8;                      // query heads per kv head (G)
+constexpr int kSwaTokens = 16;                    // tokens per tile (128 / G)
+constexpr int kSwaKeys = 144;                     // keys per tile
+constexpr int kSwaTileBlocks = kSwaKeys / kSwaBlockKeys;  // 9
+constexpr int kSwaRingBlocks = 12;                // ring capacity in blocks
+
+// Tiles [*u0, *u1) of CTA `cta` of `grid` (balanced contiguous runs).
+ATTN_HD void swa_stream_range(int cta, int grid, int ntiles, int *u0, int *u1) {
+    *u0 = static_cast<int>((static_cast<long long>(cta) * ntiles) / grid);
+    *u1 = static_cast<int>((static_cast<long long>(cta + 1) * ntiles) / grid);
+}
+
+// Block bookkeeping in load order: every block a CTA loads gets the next
+// sequence number n and lives in ring slot n mod ring.  A tile reads the
+// blocks base .. base+nb-1, whose keys start at key0 + 16*(n - base).
+struct SwaRingCursor {
+    int seq_next = 0;   // sequence number of the next block to load
+    int prev_bg = -1;   // (b*Hkv + g) of the previous tile
+    int base = 0;       // first block of the current tile
+    int first_new = 0;  // first block loaded for the current tile
+    int n_new = 0;      // blocks loaded for the current tile (nb or 1)
+};
+ATTN_HD void swa_ring_step(SwaRingCursor &c, int bg, int nb) {
+    c.first_new = c.seq_next;
+    if (bg != c.prev_bg) {
+        c.n_new = nb;
+        c.base = c.seq_next;
+    } else {
+        c.n_new = 1;
+        c.base = c.seq_next + 1 - nb;
+    }
+    c.seq_next += c.n_new;
+    c.prev_bg = bg;
+}
+// End of the blocks [base, end) that the current tile is the last to read:
+// one block when the next tile continues the same (b, g), all nb otherwise.
+ATTN_HD int swa_ring_release_end(int base, bool next_same_bg, int nb) {
+    return next_same_bg ? base + 1 : base + nb;
+}
+
+// Visible key columns [*c_lo, *c_hi] of the row at query position qpos in a
+// key tile starting at key0.
+ATTN_HD void swa_row_cols(int qpos, int key0, int window, int *c_lo, int *c_hi) {
+    int lo = qpos - window + 1;
+    if (lo < 0) lo = 0;
+    *c_lo = lo - key0;
+    *c_hi = qpos - key0;
+}
+// Whether the streaming kernel admits column c of such a row.  Interior tiles
+// (key0 >= 0, window in [114, 129]) test only columns < 32 against c_lo and
+// columns > 128 against c_hi: every other column is visible to all 128 rows.
+ATTN_HD bool swa_col_admitted(int c, int c_lo, int c_hi, bool interior) {
+    if (interior) {
+        if (c < 32) return c >= c_lo;
+        if (c > 128) return c <= c_hi;
+        return true;
+    }
+    return c >= c_lo && c <= c_hi;
+}
+
 // ---- verify split-KV geometry (GA paged): each split covers a fixed number
 // of whole pages; split s covers positions [s*chunk, (s+1)*chunk).
 ATTN_HD int verify_num_splits(int max_ctx, int chunk) { return (max_ctx + chunk - 1) / chunk; }

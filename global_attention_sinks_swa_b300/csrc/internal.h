@@ -26,11 +26,13 @@ struct PrefillMaps {
 cudaError_t launch_prefill_ga_tc(const PrefillMaps &maps, const float *sink, float *lse, int B,
                                  int T, int Hq, int Hkv, int window, float scale,
                                  unsigned int *err, cudaStream_t s);
-// tcgen05 packed-SWA prefill (G = Hq/Hkv heads x 128/G tokens per tile).
+// tcgen05 streaming SWA prefill (G = 8: 16 tokens x 8 heads per tile, window
+// in [114, 129]); one persistent CTA per SM over prefill_swa_grid() CTAs.
 cudaError_t launch_prefill_swa_tc(const PrefillMaps &maps, const float *sink, float *lse, int B,
                                   int T, int Hq, int Hkv, int window, float scale,
                                   unsigned int *err, cudaStream_t s);
 int prefill_swa_tc_supported(int G, int window);
+int prefill_swa_grid(int B, int T, int Hkv);
 
 // KV-cache appends (plain 16-byte copies).
 cudaError_t launch_ring_append(const void *k_new, const void *v_new, const int32_t *cu_q,
@@ -65,6 +67,8 @@ cudaError_t launch_verify_paged(const VerifyMaps &maps, const void *q, const int
 // Index dumps.
 cudaError_t launch_debug_prefill_visits(int32_t *visits, int mode, int T, int window, int G,
                                         cudaStream_t s);
+cudaError_t launch_debug_swa_stream_visits(int32_t *visits, int B, int T, int Hkv, int window,
+                                           int grid, cudaStream_t s);
 cudaError_t launch_debug_verify_positions(int32_t *out, int kind, const int32_t *cu_q,
                                           const int32_t *seq_lens, int B, int q_max, int window,
                                           int R, int max_pages, int page_size, cudaStream_t s);

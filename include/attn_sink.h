@@ -93,8 +93,10 @@ attn_status_t attn_check_device_error(void *stream, unsigned int *bits_out);
  *   q [B,T,Hq,D], k [B,T,Hkv,D], v [B,T,Hkv,D], o [B,T,Hq,D]   (dtype)
  *   sink [Hq] fp32 logits;  lse [B,Hq,T] fp32 natural-log LSE, or NULL
  *   window >= 1 (keys i-window+1..i);  scale > 0 (usually 1/sqrt(D))
- * Supported: ATTN_BF16 with D = 128 and Hq/Hkv in {1,2,4,8} on the tensor-core
- * path; ATTN_F32 with D in {64,128} on the fp32 CUDA-core path. */
+ * Supported: ATTN_BF16 with D = 128 and 128 % (Hq/Hkv) == 0 on the tensor cores
+ * (Hq/Hkv = 8 with window in [114, 129] on the streaming kernel, any other
+ * ratio or window on the GA-tiled kernel with window-limited tile skipping);
+ * ATTN_F32 with D in {64,128} on the fp32 CUDA-core path. */
 attn_status_t attn_swa_sink_prefill(const void *q, const void *k, const void *v, const float *sink,
                                     void *o, float *lse, int B, int T, int Hq, int Hkv, int D,
                                     int window, float scale, attn_dtype_t dtype, void *stream);
@@ -193,6 +195,18 @@ attn_status_t attn_ga_sink_verify_noalloc(const void *q, const int32_t *cu_q, co
  * exactly on visible pairs and 0 elsewhere. */
 attn_status_t attn_debug_prefill_visits(int32_t *visits, int mode, int T, int window, int G,
                                         void *stream);
+
+/* attn_debug_swa_stream_visits: the schedule of the streaming SWA prefill
+ * kernel (8 query heads per kv head, window in [114, 129]) replayed with
+ * `grid` persistent CTAs (0 = the grid the kernel launches): for every
+ * (b, kv head g) and query position i, visits[(b*Hkv+g), i, j] counts how many
+ * times a CTA's tile admits key j for query i, with the key position taken
+ * from the CTA's shared-memory ring of 16-key blocks (which block each ring
+ * slot holds).  visits [B*Hkv, T, T+1] int32 (device); column T counts
+ * admitted keys outside [0, T).  Correct schedules give 1 exactly on the
+ * visible pairs and 0 elsewhere. */
+attn_status_t attn_debug_swa_stream_visits(int32_t *visits, int B, int T, int Hkv, int window,
+                                           int grid, void *stream);
 
 /* attn_debug_verify_positions: for each request b, query t < q_max and cache
  * slot s, the absolute position the verify kernel assigns to the key it reads

@@ -1,0 +1,49 @@
+// Host-side replay of the streaming SWA prefill schedule, built from the same
+// index functions the kernel runs (index_math.cuh compiled as host code), so
+// that the CPU test suite checks the run partition, the ring bookkeeping and
+// the column masks without a GPU.  visits [B*Hkv, T, T+1]; column T counts
+// admitted keys outside [0, T).  Returns the largest number of blocks that are
+// live (loaded and not yet released) at any point of a run.
+#include "index_math.cuh"
+
+extern "C" int swa_stream_visits_host(int32_t *visits, int B, int T, int Hkv, int window,
+                                      int grid) {
+    using namespace attn;
+    const int nblk = (T + kSwaTokens - 1) / kSwaTokens;
+    const int ntiles = nblk * Hkv * B;
+    int max_live = 0;
+    for (int cta = 0; cta < grid; ++cta) {
+        int u0, u1;
+        swa_stream_range(cta, grid, ntiles, &u0, &u1);
+        SwaRingCursor cur;
+        int slot_key[kSwaRingBlocks];
+        for (int s = 0; s < kSwaRingBlocks; ++s) slot_key[s] = -(1 << 30);
+        int released = 0;  // blocks [0, released) were released
+        for (int u = u0; u < u1; ++u) {
+            const int bg = u / nblk, i0 = (u - bg * nblk) * kSwaTokens;
+            const int key0 = i0 + kSwaTokens - kSwaKeys;
+            swa_ring_step(cur, bg, kSwaTileBlocks);
+            for (int s = cur.first_new; s < cur.first_new + cur.n_new; ++s)
+                slot_key[s % kSwaRingBlocks] = key0 + kSwaBlockKeys * (s - cur.base);
+            if (cur.seq_next - released > max_live) max_live = cur.seq_next - released;
+            const bool interior = key0 >= 0;
+            for (int t = 0; t < kSwaTokens && i0 + t < T; ++t) {
+                const int qpos = i0 + t;
+                int c_lo, c_hi;
+                swa_row_cols(qpos, key0, window, &c_lo, &c_hi);
+                int32_t *row = visits + (static_cast<long>(bg) * T + qpos) * (T + 1);
+                for (int j = 0; j < kSwaTileBlocks; ++j) {
+                    const int kb = slot_key[(cur.base + j) % kSwaRingBlocks];
+                    for (int cc = 0; cc < kSwaBlockKeys; ++cc) {
+                        if (!swa_col_admitted(j * kSwaBlockKeys + cc, c_lo, c_hi, interior)) continue;
+                        const int key = kb + cc;
+                        row[(key >= 0 && key < T) ? key : T] += 1;
+                    }
+                }
+            }
+            const bool next_same = (u + 1 < u1) && ((u + 1) / nblk == bg);
+            released = swa_ring_release_end(cur.base, next_same, kSwaTileBlocks);
+        }
+    }
+    return max_live;
+}

@@ -35,6 +35,25 @@ def test_packed_swa_tiling_visits_each_visible_pair_once(T, window, G):
     np.testing.assert_array_equal(got, _expected_visits(T, window))
 
 
+@pytest.mark.parametrize("B,T,Hkv,window,grid", [
+    (1, 16, 1, 128, 0),      # one tile
+    (1, 500, 1, 128, 3),     # runs of ~10 tiles: the 12-block ring wraps
+    (2, 333, 2, 120, 5),     # runs cross (b, kv head) boundaries, ragged tail
+    (1, 1000, 2, 114, 7),    # narrowest window of the kernel
+    (2, 700, 3, 129, 0),     # widest window, the kernel's own grid
+    (1, 2048, 1, 128, 1),    # one CTA streams all 128 tiles
+])
+def test_swa_stream_schedule_visits_each_visible_pair_once(B, T, Hkv, window, grid):
+    """The streaming SWA kernel's run partition, ring-slot bookkeeping and
+    column masks, replayed: every visible (query, key) pair exactly once, no
+    other pair, no key outside the sequence."""
+    got = A.attn_debug_swa_stream_visits(B, T, Hkv, window, grid).cpu().numpy()
+    exp = _expected_visits(T, window)
+    for bg in range(B * Hkv):
+        np.testing.assert_array_equal(got[bg, :, :T], exp, err_msg=f"bg={bg}")
+        assert not got[bg, :, T].any(), f"bg={bg}: admitted keys outside [0, T)"
+
+
 @pytest.mark.parametrize("window,q_max", [(128, 4), (8, 4), (5, 1)])
 def test_ring_positions_bit_exact(window, q_max):
     R = index.ring_slots(window, q_max)

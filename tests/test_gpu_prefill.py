@@ -96,6 +96,20 @@ def test_swa_bf16_small(T, Hq, Hkv, window):
     assert_bf16_close(lse, ref_lse, "swa lse")
 
 
+@pytest.mark.parametrize("B,T,Hq,Hkv,window", [
+    (2, 2500, 16, 2, 128),   # streaming runs cross (b, kv head) boundaries
+    (1, 4096, 64, 8, 128),   # ~14 tiles per CTA: the 12-block K/V ring wraps repeatedly
+    (1, 1500, 8, 1, 114),    # narrowest window of the streaming kernel
+    (1, 1500, 8, 1, 129),    # widest window of the streaming kernel
+])
+def test_swa_stream_multi_tile_runs(B, T, Hq, Hkv, window):
+    q, k, v, sink = synth.prefill_inputs(B, T, Hq, Hkv, 128, seed=T + window + Hkv)
+    o, lse = _run("swa", q.cuda(), k.cuda(), v.cuda(), sink.cuda(), window)
+    ref, ref_lse = _oracle("swa", q, k, v, sink, window)
+    assert_bf16_close(o, ref, f"swa stream B={B} T={T} Hkv={Hkv} W={window}")
+    assert_bf16_close(lse, ref_lse, "swa stream lse")
+
+
 def test_swa_bf16_sinks_and_batch():
     q, k, v, sink = synth.prefill_inputs(3, 150, 16, 2, 128, seed=3)
     sink[0], sink[9], sink[15] = math.inf, -math.inf, -40.0

@@ -1,0 +1,65 @@
+"""The streaming SWA prefill schedule replayed on the CPU: the kernel's own
+index functions (index_math.cuh, compiled as host code) must admit every
+visible (query, key) pair exactly once across the CTA runs and the shared-
+memory ring of 16-key blocks, and never need more live blocks than the ring
+holds.  No GPU needed; the same replay runs on the device in test_gpu_index."""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "tests", "host", "swa_schedule_replay.cu")
+INC = os.path.join(ROOT, "global_attention_sinks_swa_b300", "csrc")
+LIB = os.path.join(ROOT, "_build", "libswa_schedule_replay.so")
+RING_BLOCKS = 12
+
+
+@pytest.fixture(scope="module")
+def replay():
+    os.makedirs(os.path.dirname(LIB), exist_ok=True)
+    deps = [SRC, os.path.join(INC, "index_math.cuh")]
+    if not os.path.exists(LIB) or any(os.path.getmtime(d) > os.path.getmtime(LIB) for d in deps):
+        nvcc = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
+        subprocess.run([nvcc, "-O2", "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-I", INC,
+                        SRC, "-o", LIB], check=True)
+    lib = ctypes.CDLL(LIB)
+    f = lib.swa_stream_visits_host
+    f.argtypes = [np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")] + [ctypes.c_int] * 5
+    f.restype = ctypes.c_int
+
+    def run(B, T, Hkv, window, grid):
+        visits = np.zeros((B * Hkv, T, T + 1), np.int32)
+        live = f(visits, B, T, Hkv, window, grid)
+        return visits, live
+    return run
+
+
+def _expected(T, window):
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    return ((j <= i) & (j >= i - window + 1)).astype(np.int32)
+
+
+@pytest.mark.parametrize("B,T,Hkv,window,grid", [
+    (1, 1, 1, 128, 1), (1, 16, 1, 128, 1), (1, 17, 1, 128, 2), (1, 500, 1, 128, 3),
+    (2, 333, 2, 120, 5), (1, 1000, 2, 114, 7), (2, 700, 3, 129, 148), (1, 2048, 1, 128, 1),
+    (3, 257, 2, 128, 4), (1, 3000, 2, 128, 148),
+])
+def test_schedule_admits_each_visible_pair_once(replay, B, T, Hkv, window, grid):
+    nblk = (T + 15) // 16
+    grid = min(grid, nblk * Hkv * B)
+    visits, live = replay(B, T, Hkv, window, grid)
+    exp = _expected(T, window)
+    for bg in range(B * Hkv):
+        np.testing.assert_array_equal(visits[bg, :, :T], exp, err_msg=f"bg={bg}")
+        assert not visits[bg, :, T].any()
+    assert live <= RING_BLOCKS
+
+
+def test_replay_catches_a_wrong_window(replay):
+    """A schedule built for W=128 does not pass as W=127 (the check has teeth)."""
+    visits, _ = replay(1, 300, 1, 128, 2)
+    assert not np.array_equal(visits[0, :, :300], _expected(300, 127))
