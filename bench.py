@@ -71,8 +71,16 @@ def load_peaks():
 
 
 def source_sha(rel: str) -> str:
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel file together with every header of the library, so
+    that recorded counters go stale whenever the compiled kernel could change."""
+    import glob
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "global_attention_sinks_swa_b300", "csrc")
+    for path in [os.path.join(ROOT, rel)] + sorted(glob.glob(os.path.join(csrc, "*.cuh")) +
+                                                   glob.glob(os.path.join(csrc, "*.h"))):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel_file: str, name: str):
@@ -501,8 +509,8 @@ def main():
                        "l2": "inputs larger than L2 (1.2 GB per set, 2 rotating sets)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_source": peak_src,
-                         "traffic": ncu_traffic("global_attention_sinks_swa_b300/csrc/prefill_tc.cu",
-                                                "prefill_swa_kernel"),
+                         "traffic": ncu_traffic("global_attention_sinks_swa_b300/csrc/prefill_swa.cu",
+                                                "prefill_swa_stream_kernel"),
                          "algorithmic_bytes": prefill_min_bytes(),
                          "tensor_frac": flop / (ms * 1e-3) / 1e12 / tf_burst},
             "clocks": clocks.summary(),
