@@ -274,16 +274,22 @@ ATTN_EXPORT attn_status_t attn_swa_sink_verify(const void *q, const int32_t *cu_
     unsigned *err = device_error_word();
     if (!err) return fail(ATTN_ERR_CUDA, "no CUDA device / error word unavailable");
     attn::VerifyMaps maps;
+    const bool tc = attn::verify_ring_tc_supported(Hq / Hkv, ring_slots, q_max) != 0;
     uint64_t dims[4] = {128, static_cast<uint64_t>(ring_slots), static_cast<uint64_t>(Hkv),
                         static_cast<uint64_t>(B)};
     uint64_t strides[3] = {256, static_cast<uint64_t>(ring_slots) * 256,
                            static_cast<uint64_t>(Hkv) * ring_slots * 256};
-    uint32_t box[4] = {64, static_cast<uint32_t>(attn::kVerifyBlock), 1, 1};
+    // tensor-core kernel: the whole ring in one box; otherwise 64-slot blocks
+    uint32_t box[4] = {64, static_cast<uint32_t>(tc ? attn::kVerifyRingKeys : attn::kVerifyBlock), 1,
+                       1};
     if (!make_map_4d(&maps.k, ring_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, strides, box) ||
         !make_map_4d(&maps.v, ring_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, strides, box))
         return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the ring maps");
-    cudaError_t e = attn::launch_verify_ring(maps, q, cu_q, seq_lens, sink, o, B, Hq, Hkv, window,
-                                             ring_slots, q_max, scale, err, as_stream(stream));
+    cudaError_t e =
+        tc ? attn::launch_verify_ring_tc(maps, q, cu_q, seq_lens, sink, o, B, Hq, Hkv, window,
+                                         ring_slots, q_max, scale, err, as_stream(stream))
+           : attn::launch_verify_ring(maps, q, cu_q, seq_lens, sink, o, B, Hq, Hkv, window,
+                                      ring_slots, q_max, scale, err, as_stream(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "swa verify launch");
 }
 

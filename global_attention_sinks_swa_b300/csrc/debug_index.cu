@@ -88,10 +88,12 @@ __global__ void verify_positions_kernel(int32_t *out, int kind, const int32_t *c
     const int L = seq_lens[b], q_len = cu_q[b + 1] - cu_q[b];
     const int i = L - q_len + t;  // query position
     if (kind == 0) {
+        // visibility as the tensor-core ring kernel decides it (two slot
+        // intervals), positions as both ring kernels compute them
+        const RingVisible vis = ring_visible_slots(L, R, window, i);
         for (int s = threadIdx.x; s < R; s += blockDim.x) {
             const int p = ring_slot_position(s, L, R);
-            out[(static_cast<long>(b) * q_max + t) * R + s] =
-                (t < q_len && p >= 0 && key_visible(i, p, window)) ? p : -1;
+            out[(static_cast<long>(b) * q_max + t) * R + s] = (t < q_len && vis.contains(s)) ? p : -1;
         }
     } else {
         const long n = static_cast<long>(max_pages) * page_size;

@@ -18,18 +18,48 @@
 
 namespace attn {
 
+// (bitwise operators: no branch per element in the kernels' unrolled masks)
 ATTN_HD bool key_visible(int i, int j, int window) {
-    return j >= 0 && j <= i && (window <= 0 || j > i - window);
+    return (j >= 0) & (j <= i) & ((window <= 0) | (j > i - window));
 }
 
 // The position held by ring slot `s` once positions 0..L-1 were written into
 // a ring of R slots: the unique p in [L-R, L) with p = s (mod R), or -1.
-ATTN_HD int ring_slot_position(int s, int L, int R) {
-    int base = L - R;
-    int r = (s - base) % R;
-    if (r < 0) r += R;
-    int p = base + r;
+// With r0 = L mod R (computed once per request), slots r0..R-1 hold
+// L-R .. L-R+(R-1-r0) and slots 0..r0-1 hold L-r0 .. L-1.
+ATTN_HD int ring_slot_position_r0(int s, int L, int R, int r0) {
+    const int p = s + (s >= r0 ? L - R - r0 : L - r0);
     return p >= 0 ? p : -1;
+}
+ATTN_HD int ring_slot_position(int s, int L, int R) {
+    return ring_slot_position_r0(s, L, R, L % R);
+}
+// The ring slots visible from query position qpos (window W) once positions
+// 0..L-1 were written: those holding positions in [max(0, qpos-W+1), qpos].
+// Since slots r0..R-1 and 0..r0-1 each hold increasing positions, they are at
+// most two intervals [a1, a1+n1) and [a2, a2+n2).  contains() is two unsigned
+// compares and a bitwise OR: no branch per slot.
+struct RingVisible {
+    int a1, n1, a2, n2;
+    ATTN_HD bool contains(int s) const {
+        return (static_cast<unsigned>(s - a1) < static_cast<unsigned>(n1)) |
+               (static_cast<unsigned>(s - a2) < static_cast<unsigned>(n2));
+    }
+};
+ATTN_HD RingVisible ring_visible_slots(int L, int R, int window, int qpos) {
+    const int r0 = L % R;
+    int lo = qpos - window + 1;
+    if (lo < 0) lo = 0;
+    const int a1 = lo - (L - R - r0) > r0 ? lo - (L - R - r0) : r0;
+    const int b1 = qpos - (L - R - r0) < R - 1 ? qpos - (L - R - r0) : R - 1;
+    const int a2 = lo - (L - r0) > 0 ? lo - (L - r0) : 0;
+    const int b2 = qpos - (L - r0) < r0 - 1 ? qpos - (L - r0) : r0 - 1;
+    RingVisible v;
+    v.a1 = a1;
+    v.n1 = b1 >= a1 ? b1 - a1 + 1 : 0;
+    v.a2 = a2;
+    v.n2 = b2 >= a2 ? b2 - a2 + 1 : 0;
+    return v;
 }
 
 // ---- GA prefill tiling: BM query rows per tile, BN keys per key tile.
@@ -133,7 +163,7 @@ ATTN_HD bool swa_col_admitted(int c, int c_lo, int c_hi, bool interior) {
         if (c > 128) return c <= c_hi;
         return true;
     }
-    return c >= c_lo && c <= c_hi;
+    return (c >= c_lo) & (c <= c_hi);
 }
 
 // ---- verify split-KV geometry (GA paged): each split covers a fixed number

@@ -54,6 +54,14 @@ constexpr int kVerifyRows = 32;       // q_max * G rows per (request, kv head), 
 constexpr int kVerifyBlock = 64;      // keys per pipeline stage (one GA page)
 constexpr int kVerifyChunkPages = 64; // pages per split of the GA context (4096 tokens)
 
+// tcgen05 ring verify: one CTA per (request, kv head), the whole ring in one
+// pass; K/V maps with a box of kVerifyRingKeys slot rows.
+constexpr int kVerifyRingKeys = 144;  // ring slots covered (R <= 144), multiple of 16
+int verify_ring_tc_supported(int G, int R, int q_max);
+cudaError_t launch_verify_ring_tc(const VerifyMaps &maps, const void *q, const int32_t *cu_q,
+                                  const int32_t *seq_lens, const float *sink, void *o, int B,
+                                  int Hq, int Hkv, int window, int R, int q_max, float scale,
+                                  unsigned int *err, cudaStream_t s);
 cudaError_t launch_verify_ring(const VerifyMaps &maps, const void *q, const int32_t *cu_q,
                                const int32_t *seq_lens, const float *sink, void *o, int B, int Hq,
                                int Hkv, int window, int R, int q_max, float scale,

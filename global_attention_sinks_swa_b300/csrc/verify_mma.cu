@@ -33,16 +33,21 @@ constexpr int kHalfBytes = kVerifyBlock * 128;  // 64 rows x 128 B (64 bf16)
 constexpr int kStageBytes = 4 * kHalfBytes;      // K and V, two D halves each
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kErrPage = 0x1u, kErrCtx = 0x2u, kErrQlen = 0x4u, kErrWait = 0x8u;
+constexpr int kMergeStride = kD + 8;     // floats per row of the key-half merge buffer
+constexpr int kStageRowBytes = 2 * kD + 16;  // bytes per row of the bf16 output staging
 
 struct __align__(1024) VerifySmem {
-    uint8_t k[kStages][2][kHalfBytes];
-    uint8_t v[kStages][2][kHalfBytes];
+    uint8_t k[kStages][2][kHalfBytes];  // after the loop: the key-half merge buffer
+    uint8_t v[kStages][2][kHalfBytes];  // after the loop: the bf16 output staging
     uint8_t q[2][kVerifyRows * 128];
     uint64_t full[kStages];
     uint64_t empty[kStages];
     float merge_ml[2][16][2];
     int abort;
 };
+
+static_assert(2 * 16 * kMergeStride * sizeof(float) <= sizeof(VerifySmem::k), "merge buffer");
+static_assert(kVerifyRows * kStageRowBytes <= sizeof(VerifySmem::v), "output staging");
 
 // Byte offset of element (row, d) inside a 128B-swizzled [rows][64] half tile;
 // d a multiple of 8.
@@ -54,12 +59,12 @@ struct KeySource {
     // ring: blocks cover slots [64*blk, 64*blk+64) of the R-slot ring
     // paged: block = one page of page_table[b][pb + blk]
     int kind;        // 0 ring, 1 paged
-    int L, R;        // sequence length, ring slots
+    int L, R, r0;    // sequence length, ring slots, L mod R
     int pb;          // first page-table index of this split (paged)
     __device__ __forceinline__ int position(int blk, int c) const {
         if (kind == 0) {
             const int s = blk * kVerifyBlock + c;
-            return s < R ? ring_slot_position(s, L, R) : -1;
+            return s < R ? ring_slot_position_r0(s, L, R, r0) : -1;
         }
         return (pb + blk) * kVerifyBlock + c;
     }
@@ -97,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (threadIdx.x == 0 && split == 0 && g == 0) atomicOr(err, kErrQlen);
         return;
     }
-    KeySource src{kind, L, R, 0};
+    KeySource src{kind, L, R, kind == 0 && R > 0 ? L % R : 0, 0};
     int nblk;
     if (kind == 0) {
         if (L < q_len) {
@@ -217,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             sm.abort = 1;
             break;
         }
-        if (active) {
+        // ring: a warp whose 32 keys of this block all lie past the last slot skips it
+        if (active && (kind != 0 || blk * kVerifyBlock + kh * 32 < R)) {
             // S = Q K^T for this warp's 16 rows x 32 keys
             float s[4][4];
 #pragma unroll
@@ -305,14 +311,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         lrow[h2] += __shfl_xor_sync(0xffffffffu, lrow[h2], 2);
     }
     ptx::named_bar_sync(1, kConsumers * 32);  // every warp is done with the stage buffers
-    float *mo = reinterpret_cast<float *>(sm.k[0][0]) + mt * 16 * kD;  // [16][128] per m tile
+    // rows padded to kMergeStride floats: float2 writes of 8 rows hit distinct banks
+    float *mo = reinterpret_cast<float *>(sm.k[0][0]) + mt * 16 * kMergeStride;
     if (kh == 1 && active) {
 #pragma unroll
         for (int n = 0; n < 16; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int rr = (lane >> 2) + (e >> 1) * 8, d = n * 8 + 2 * (lane & 3) + (e & 1);
-                mo[rr * kD + d] = oacc[n][e];
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int rr = (lane >> 2) + h2 * 8, d = n * 8 + 2 * (lane & 3);
+                *reinterpret_cast<float2 *>(mo + rr * kMergeStride + d) =
+                    make_float2(oacc[n][2 * h2], oacc[n][2 * h2 + 1]);
             }
         if ((lane & 3) == 0)
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -321,53 +329,68 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
     }
     ptx::named_bar_sync(1, kConsumers * 32);
-    if (kh == 1 || !active || sm.abort) return;
-
-    float sa[2], sb[2];
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-        const int rr = (lane >> 2) + h2 * 8;
-        const float mb = sm.merge_ml[mt][rr][0], lb = sm.merge_ml[mt][rr][1];
-        const float mm = merge_scale(mrow[h2], mb, &sa[h2], &sb[h2]);
-        lrow[h2] = lrow[h2] * sa[h2] + lb * sb[h2];
-        mrow[h2] = mm;
-    }
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int rr = (lane >> 2) + (e >> 1) * 8, d = n * 8 + 2 * (lane & 3) + (e & 1);
-            oacc[n][e] = oacc[n][e] * sa[e >> 1] + mo[rr * kD + d] * sb[e >> 1];
-        }
-
-    if (finalize) {
-        // add the sink once and write bf16 rows
+    const bool lead = kh == 0 && active && !sm.abort;  // warps that hold the merged rows
+    if (lead) {
+        float sa[2], sb[2];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-            const int r = mt * 16 + (lane >> 2) + h2 * 8;
-            const int t = r / G, hh = r % G;
-            if (t >= q_len) continue;
-            const float sig = sink[g * G + hh];
-            float inv;
-            if (isinf(sig) && sig > 0.f) {
-                inv = 0.f;
-            } else {
-                const float s2 = sig * kLog2e;
-                float ssa, ssb;
-                const float mm = merge_scale(mrow[h2], s2, &ssa, &ssb);
-                (void)mm;
-                const float z = lrow[h2] * ssa + ssb;
-                inv = ssa / z;
-            }
-            __nv_bfloat16 *orow = o + (static_cast<long>(r0 + t) * Hq + g * G + hh) * kD;
+            const int rr = (lane >> 2) + h2 * 8;
+            const float mb = sm.merge_ml[mt][rr][0], lb = sm.merge_ml[mt][rr][1];
+            const float mm = merge_scale(mrow[h2], mb, &sa[h2], &sb[h2]);
+            lrow[h2] = lrow[h2] * sa[h2] + lb * sb[h2];
+            mrow[h2] = mm;
+        }
 #pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                const int d = n * 8 + 2 * (lane & 3);
-                *reinterpret_cast<uint32_t *>(orow + d) =
-                    ptx::pack_bf16x2(oacc[n][2 * h2] * inv, oacc[n][2 * h2 + 1] * inv);
+        for (int n = 0; n < 16; ++n)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int rr = (lane >> 2) + h2 * 8, d = n * 8 + 2 * (lane & 3);
+                const float2 x = *reinterpret_cast<const float2 *>(mo + rr * kMergeStride + d);
+                oacc[n][2 * h2] = oacc[n][2 * h2] * sa[h2] + x.x * sb[h2];
+                oacc[n][2 * h2 + 1] = oacc[n][2 * h2 + 1] * sa[h2] + x.y * sb[h2];
+            }
+    }
+
+    if (finalize) {
+        // add the sink once; bf16 rows staged in shared memory (rows padded to
+        // kStageRowBytes), then written with coalesced 16-byte stores
+        uint8_t *ost = sm.v[0][0];
+        if (lead) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int r = mt * 16 + (lane >> 2) + h2 * 8;
+                const int hh = r % G;
+                const float sig = sink[g * G + hh];
+                float inv;
+                if (isinf(sig) && sig > 0.f) {
+                    inv = 0.f;
+                } else {
+                    const float s2 = sig * kLog2e;
+                    float ssa, ssb;
+                    merge_scale(mrow[h2], s2, &ssa, &ssb);
+                    const float z = lrow[h2] * ssa + ssb;
+                    inv = ssa / z;
+                }
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    const int d = n * 8 + 2 * (lane & 3);
+                    *reinterpret_cast<uint32_t *>(ost + r * kStageRowBytes + d * 2) =
+                        ptx::pack_bf16x2(oacc[n][2 * h2] * inv, oacc[n][2 * h2 + 1] * inv);
+                }
             }
         }
-    } else {
+        ptx::named_bar_sync(1, kConsumers * 32);
+        if (!sm.abort) {
+            for (int x = threadIdx.x; x < kVerifyRows * 16; x += kConsumers * 32) {
+                const int r = x >> 4, c = x & 15;
+                if (r >= q_len * G) break;
+                const int t = r / G, hh = r % G;
+                *reinterpret_cast<uint4 *>(o + (static_cast<long>(r0 + t) * Hq + g * G + hh) * kD +
+                                           c * 8) =
+                    *reinterpret_cast<const uint4 *>(ost + r * kStageRowBytes + c * 16);
+            }
+        }
+    } else if (lead) {
         // partial state of this split: m (log2 units), l, unnormalised o
         const long unit = (static_cast<long>(b) * Hkv + g) * nsplit + split;
         float *wo = ws_o + unit * kVerifyRows * kD;

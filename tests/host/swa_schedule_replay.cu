@@ -47,3 +47,11 @@ extern "C" int swa_stream_visits_host(int32_t *visits, int B, int T, int Hkv, in
     }
     return max_live;
 }
+
+// Ring visibility as the tensor-core verify kernel computes it: out[s] = the
+// position held by slot s if visible from query position qpos, else -1.
+extern "C" void ring_visible_host(int32_t *out, int L, int R, int window, int qpos) {
+    using namespace attn;
+    const RingVisible vis = ring_visible_slots(L, R, window, qpos);
+    for (int s = 0; s < R; ++s) out[s] = vis.contains(s) ? ring_slot_position(s, L, R) : -1;
+}

@@ -19,14 +19,14 @@ Hq, Hkv, D, W, QMAX, PAGE = 64, 8, 128, 128, 4, 64
 R = index.ring_slots(W, QMAX)
 
 
-def ring_from_history(k_hist, seq_lens):
-    """[B,Lmax,Hkv,D] -> ring [B,Hkv,R,D] holding positions max(0,L-R)..L-1."""
-    B = k_hist.shape[0]
-    ring = torch.zeros(B, Hkv, R, D, dtype=k_hist.dtype)
+def ring_from_history(k_hist, seq_lens, slots=R):
+    """[B,Lmax,Hkv,D] -> ring [B,Hkv,slots,D] holding positions max(0,L-slots)..L-1."""
+    B, _, hkv, _ = k_hist.shape
+    ring = torch.zeros(B, hkv, slots, D, dtype=k_hist.dtype)
     for b in range(B):
         L = int(seq_lens[b])
-        for p in range(max(0, L - R), L):
-            ring[b, :, index.ring_slot(p, R)] = k_hist[b, p]
+        for p in range(max(0, L - slots), L):
+            ring[b, :, index.ring_slot(p, slots)] = k_hist[b, p]
     return ring
 
 
@@ -99,6 +99,36 @@ CASES = [
 def test_swa_ring_verify(seq_lens, q_lens):
     P = make_problem(seq_lens, q_lens, seed=sum(seq_lens))
     assert_bf16_close(run_ring(P), ref(P, W), "ring verify")
+
+
+@pytest.mark.parametrize("window,hq,hkv", [
+    (8, 64, 8),     # tensor-core kernel, ring of 11 slots
+    (141, 64, 8),   # tensor-core kernel, ring of 144 slots (its largest)
+    (200, 64, 8),   # ring of 203 slots: mma.sync kernel
+    (128, 32, 8),   # 4 q-heads per kv head: mma.sync kernel
+    (5, 16, 4),     # 4 q-heads per kv head, small window
+])
+def test_swa_ring_verify_both_kernels(window, hq, hkv):
+    """The ring verify on both of its kernels (tcgen05 for 8 q-heads per kv head
+    and rings <= 144 slots, mma.sync otherwise) against the oracle."""
+    seq_lens = np.array([3, 9, 150, 151, 260, 1000], np.int32)
+    q_lens = np.array([3, 4, 4, 1, 2, 4], np.int32)
+    B, Lmax = len(seq_lens), int(seq_lens.max())
+    seed = window + hq
+    k_hist = synth.normal((B, Lmax, hkv, D), seed)
+    v_hist = synth.normal((B, Lmax, hkv, D), seed + 1)
+    cu_q = synth.cu_seqlens(q_lens)
+    q = synth.normal((int(cu_q[-1]), hq, D), seed + 2)
+    sink = synth.sink_logits(hq, seed + 3)
+    R = index.ring_slots(window, QMAX)
+    rk = ring_from_history(k_hist, seq_lens, R).cuda()
+    rv = ring_from_history(v_hist, seq_lens, R).cuda()
+    o = A.attn_swa_sink_verify(q.cuda(), torch.from_numpy(cu_q).cuda(), rk, rv,
+                               torch.from_numpy(seq_lens).cuda(), sink.cuda(), window=window,
+                               q_max=QMAX)
+    assert A.attn_check_device_error() == 0
+    ref_o = oracle.verify(q, cu_q, k_hist, v_hist, seq_lens, sink, window)
+    assert_bf16_close(o, ref_o, f"ring verify W={window} G={hq // hkv}")
 
 
 @pytest.mark.parametrize("seq_lens,q_lens", CASES + [([4097, 9000, 64, 65], [4, 3, 1, 4])])

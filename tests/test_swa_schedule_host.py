@@ -1,8 +1,11 @@
-"""The streaming SWA prefill schedule replayed on the CPU: the kernel's own
-index functions (index_math.cuh, compiled as host code) must admit every
-visible (query, key) pair exactly once across the CTA runs and the shared-
-memory ring of 16-key blocks, and never need more live blocks than the ring
-holds.  No GPU needed; the same replay runs on the device in test_gpu_index."""
+"""Index logic of the kernels replayed on the CPU, from the kernels' own
+functions (index_math.cuh compiled as host code):
+- the streaming SWA prefill schedule must admit every visible (query, key)
+  pair exactly once across the CTA runs and the shared-memory ring of 16-key
+  blocks, and never need more live blocks than the ring holds;
+- the ring verify's visible slots (two slot intervals) must be exactly the
+  slots holding positions in the query's window.
+No GPU needed; the same functions run on the device in test_gpu_index."""
 import ctypes
 import os
 import subprocess
@@ -29,11 +32,14 @@ def replay():
     f = lib.swa_stream_visits_host
     f.argtypes = [np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")] + [ctypes.c_int] * 5
     f.restype = ctypes.c_int
+    lib.ring_visible_host.argtypes = [np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")] + [ctypes.c_int] * 4
+    lib.ring_visible_host.restype = None
 
     def run(B, T, Hkv, window, grid):
         visits = np.zeros((B * Hkv, T, T + 1), np.int32)
         live = f(visits, B, T, Hkv, window, grid)
         return visits, live
+    run.ring_visible = lib.ring_visible_host
     return run
 
 
@@ -63,3 +69,25 @@ def test_replay_catches_a_wrong_window(replay):
     """A schedule built for W=128 does not pass as W=127 (the check has teeth)."""
     visits, _ = replay(1, 300, 1, 128, 2)
     assert not np.array_equal(visits[0, :, :300], _expected(300, 127))
+
+
+def test_ring_visible_slots_match_the_definition(replay):
+    """Slot s of a ring of R slots, after positions 0..L-1 were written, holds
+    the p in [L-R, L) with p = s mod R; it is visible from query position i iff
+    max(0, i-W+1) <= p <= i."""
+    rng = np.random.default_rng(7)
+    for _ in range(3000):
+        q_max = int(rng.integers(1, 5))
+        W = int(rng.integers(1, 142))
+        R = W + q_max - 1 + int(rng.integers(0, 3))
+        L = int(rng.integers(1, 4 * R + 10))
+        q_len = int(rng.integers(1, min(q_max, L) + 1))
+        t = int(rng.integers(0, q_len))
+        i = L - q_len + t
+        got = np.zeros(R, np.int32)
+        replay.ring_visible(got, L, R, W, i)
+        exp = np.full(R, -1, np.int32)
+        for p in range(max(0, L - R), L):
+            if max(0, i - W + 1) <= p <= i:
+                exp[p % R] = p
+        np.testing.assert_array_equal(got, exp, err_msg=f"L={L} R={R} W={W} i={i}")
