@@ -242,6 +242,36 @@ ATTN_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
 }
 ATTN_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 16-lane shapes (16 TMEM lanes from the address's lane; thread i of the warp
+// serves lanes i/4 and i/4 + 8).  16x256b: per repetition k, registers
+// {lane i/4: columns 8k + 2(i%4), +1; lane i/4 + 8: the same two columns}.
+// 16x128b: per repetition k, {lane i/4: column 4k + i%4; lane i/4 + 8: same}.
+ATTN_DEV void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : ATTN_R8(0), ATTN_R8(8), ATTN_R8(16), ATTN_R8(24)
+        : "r"(taddr));
+}
+ATTN_DEV void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : ATTN_R8(0)
+                 : "r"(taddr));
+}
+ATTN_DEV void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        ATTN_I8(0), ATTN_I8(8)
+        : "memory");
+}
+ATTN_DEV void tmem_st_16x128b_x2(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 // ------------------------------------------------- mma.sync / ldmatrix (sm80+)
 ATTN_DEV void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
