@@ -87,6 +87,20 @@ bool make_map_4d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, const
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// [rows, H, 128] bf16 tensor viewed as (128, H, rows) with a box of (64, bh, 1).
+bool map_3d(CUtensorMap *m, const void *base, uint64_t rows, int H, uint32_t bh) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t gd[3] = {128, static_cast<cuuint64_t>(H), rows};
+    cuuint64_t gs[2] = {256, static_cast<cuuint64_t>(H) * 256};
+    cuuint32_t bx[3] = {64, bh, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gd, gs, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
 // [B,T,H,D] bf16 tensor viewed as (D, H, T, B) with a box of (64, bh, bt, 1).
@@ -285,8 +299,13 @@ ATTN_EXPORT attn_status_t attn_swa_sink_verify(const void *q, const int32_t *cu_
     if (!make_map_4d(&maps.k, ring_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, strides, box) ||
         !make_map_4d(&maps.v, ring_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, strides, box))
         return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the ring maps");
+    // q [cu_q[B], Hq, D] seen as B*q_max rows: an upper bound of cu_q[B] that
+    // only bounds the map; the kernel reads the rows of its request and
+    // rejects a request whose rows would pass B*q_max
+    if (tc && !map_3d(&maps.q, q, static_cast<uint64_t>(B) * q_max, Hq, Hq / Hkv))
+        return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the q map");
     cudaError_t e =
-        tc ? attn::launch_verify_ring_tc(maps, q, cu_q, seq_lens, sink, o, B, Hq, Hkv, window,
+        tc ? attn::launch_verify_ring_tc(maps, cu_q, seq_lens, sink, o, B, Hq, Hkv, window,
                                          ring_slots, q_max, scale, err, as_stream(stream))
            : attn::launch_verify_ring(maps, q, cu_q, seq_lens, sink, o, B, Hq, Hkv, window,
                                       ring_slots, q_max, scale, err, as_stream(stream));

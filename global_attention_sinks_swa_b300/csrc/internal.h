@@ -49,6 +49,7 @@ cudaError_t launch_paged_append(const void *k_new, const void *v_new, const int3
 struct VerifyMaps {
     CUtensorMap k;  // [.., Hkv, 64-row block, D] view of the ring or page pool
     CUtensorMap v;
+    CUtensorMap q;  // tensor-core ring kernel: [B*q_max, Hq, D] view of q (boxes of 8 heads)
 };
 constexpr int kVerifyRows = 32;       // q_max * G rows per (request, kv head), padded
 constexpr int kVerifyBlock = 64;      // keys per pipeline stage (one GA page)
@@ -58,7 +59,7 @@ constexpr int kVerifyChunkPages = 64; // pages per split of the GA context (4096
 // pass; K/V maps with a box of kVerifyRingKeys slot rows.
 constexpr int kVerifyRingKeys = 144;  // ring slots covered (R <= 144), multiple of 16
 int verify_ring_tc_supported(int G, int R, int q_max);
-cudaError_t launch_verify_ring_tc(const VerifyMaps &maps, const void *q, const int32_t *cu_q,
+cudaError_t launch_verify_ring_tc(const VerifyMaps &maps, const int32_t *cu_q,
                                   const int32_t *seq_lens, const float *sink, void *o, int B,
                                   int Hq, int Hkv, int window, int R, int q_max, float scale,
                                   unsigned int *err, cudaStream_t s);

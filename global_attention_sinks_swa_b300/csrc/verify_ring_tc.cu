@@ -10,8 +10,7 @@
 //
 // One CTA per (request, kv head).  Its q_len x G query rows (G = 8 heads of
 // the kv group, q_len <= 4 tokens) meet the whole ring in one pass:
-//   - the softmax warps copy Q (q_len tokens x 8 heads) into shared memory in
-//     the 128-byte-swizzled layout a TMA box would have; TMA loads K of all R
+//   - TMA loads Q (one box of 8 heads per token, q_len boxes) and K of all R
 //     slots as one box of 144 rows per D half (rows past the ring read 0), and
 //     V into the same buffer once S has read K, while the softmax runs -- 44 KB
 //     of shared memory and <= 102 registers per thread let 4 CTAs share an SM,
@@ -69,12 +68,13 @@ struct __align__(1024) Smem {
 };
 
 __global__ void __launch_bounds__(kThreads, 4)
-    verify_ring_tc_kernel(const __nv_bfloat16 *__restrict__ q,
+    verify_ring_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                           const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv,
                           const int32_t *__restrict__ cu_q, const int32_t *__restrict__ seq_lens,
                           const float *__restrict__ sink, __nv_bfloat16 *__restrict__ o, int Hq,
-                          int Hkv, int window, int R, int q_max, float scale, unsigned *err) {
+                          int Hkv, int window, int R, int q_max, int q_rows, float scale,
+                          unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 
     // ---- validate the request (uniform across the CTA)
     if (q_len <= 0) return;
-    if (q_len > q_max || q_len > kMaxTokens) {
+    if (q_len > q_max || q_len > kMaxTokens || r0 < 0 || r0 + q_len > q_rows) {
         if (threadIdx.x == 0 && g == 0) atomicOr(err, 0x4u);
         return;
     }
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&sm.q_ready, 4);  // one arrival per softmax warp
+        ptx::mbar_init(&sm.q_ready, 1);
         ptx::mbar_init(&sm.k_full, 1);
         ptx::mbar_init(&sm.v_full, 1);
         ptx::mbar_init(&sm.mma_done, 1);
@@ -119,8 +119,15 @@ __global__ void __launch_bounds__(kThreads, 4)
         // ----------------------------------------------- TMA loads and MMAs
         if (lane == 0 && !skip) {
             bool ok = true, issued = false;
+            ptx::prefetch_tmap(&tmq);
             ptx::prefetch_tmap(&tmk);
             ptx::prefetch_tmap(&tmv);
+            // Q: token t's 8 heads (1 KB per D half) at row group t
+            ptx::mbar_arrive_expect_tx(&sm.q_ready, 2 * q_len * kG * kHalfRowBytes);
+            for (int tt = 0; tt < q_len; ++tt)
+                for (int hf = 0; hf < 2; ++hf)
+                    ptx::tma_load_3d(sm.q[hf] + tt * kG * kHalfRowBytes, &tmq, hf * 64, g * kG, r0 + tt,
+                                     &sm.q_ready);
             ptx::mbar_arrive_expect_tx(&sm.k_full, 2 * kKHalf);
             for (int hf = 0; hf < 2; ++hf) ptx::tma_load_4d(sm.kv[hf], &tmk, hf * 64, 0, g, b, &sm.k_full);
             // S = Q K^T: A rows 32t + j (j < 8) read token t, head j (8-row
@@ -155,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 4)
             }
             if (!ok) atomicOr(err, kErrWait);
             // copies and MMAs in flight finish before the CTA may exit (bounded)
+            ptx::mbar_wait(&sm.q_ready, 0);
             ptx::mbar_wait(&sm.k_full, 0);
             if (issued) ptx::mbar_wait(&sm.v_full, 0);
             if (issued) {
@@ -179,19 +187,6 @@ __global__ void __launch_bounds__(kThreads, 4)
         const int h = g * kG + qrow;
         const float sig = sink[h];
         const float sl2 = scale * kLog2e;
-        // Q rows t*8+hh -> shared memory, 128-byte swizzled like a TMA box
-        for (int x = threadIdx.x; x < kMaxTokens * kG * 16; x += 4 * 32) {
-            const int row = x >> 4, c = x & 15;  // row, 16-byte chunk of its 256 bytes
-            const int tt = row / kG, hh = row % kG;
-            if (tt < q_len)
-                *reinterpret_cast<uint4 *>(sm.q[c >> 3] + row * kHalfRowBytes +
-                                           (((c & 7) ^ (row & 7)) << 4)) =
-                    *reinterpret_cast<const uint4 *>(
-                        q + (static_cast<long>(r0 + tt) * Hq + g * kG + hh) * 128 + c * 8);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.q_ready);
         bool ok = ptx::mbar_wait_warp(&sm.s_full, 0);
         float mb = 0.f, l = 0.f;
         if (ok) {
@@ -301,7 +296,7 @@ int verify_ring_tc_supported(int G, int R, int q_max) {
     return G == vring::kG && R >= 1 && R <= vring::kN && q_max >= 1 && q_max <= vring::kMaxTokens;
 }
 
-cudaError_t launch_verify_ring_tc(const VerifyMaps &maps, const void *q, const int32_t *cu_q,
+cudaError_t launch_verify_ring_tc(const VerifyMaps &maps, const int32_t *cu_q,
                                   const int32_t *seq_lens, const float *sink, void *o, int B,
                                   int Hq, int Hkv, int window, int R, int q_max, float scale,
                                   unsigned int *err, cudaStream_t s) {
@@ -312,8 +307,8 @@ cudaError_t launch_verify_ring_tc(const VerifyMaps &maps, const void *q, const i
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     vring::verify_ring_tc_kernel<<<dim3(Hkv, B), vring::kThreads, smem, s>>>(
-        static_cast<const __nv_bfloat16 *>(q), maps.k, maps.v, cu_q, seq_lens, sink,
-        static_cast<__nv_bfloat16 *>(o), Hq, Hkv, window, R, q_max, scale, err);
+        maps.q, maps.k, maps.v, cu_q, seq_lens, sink, static_cast<__nv_bfloat16 *>(o), Hq, Hkv,
+        window, R, q_max, B * q_max, scale, err);
     return cudaGetLastError();
 }
 
