@@ -325,14 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             float x[kN];
             tmem_load_row<kN>(tS, x);
+            // selects, not conditional stores: a branch per column costs
+            // far more than the compare
             if (interior) {
 #pragma unroll
-                for (int c = 0; c < kN; ++c)
-                    if (!swa_col_admitted(c, c_lo, c_hi, true)) x[c] = -INFINITY;
+                for (int c = 0; c < kN; ++c) x[c] = swa_col_admitted(c, c_lo, c_hi, true) ? x[c] : -INFINITY;
             } else {
 #pragma unroll
-                for (int c = 0; c < kN; ++c)
-                    if (!swa_col_admitted(c, c_lo, c_hi, false)) x[c] = -INFINITY;
+                for (int c = 0; c < kN; ++c) x[c] = swa_col_admitted(c, c_lo, c_hi, false) ? x[c] : -INFINITY;
             }
             // row max of the raw scores (scale > 0 commutes with max), seeded
             // with the sink logit; four independent partial maxima

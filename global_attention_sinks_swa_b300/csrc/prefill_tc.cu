@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ga_tile_needs_mask(qs, j, window)) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
-                    if (!key_visible(qpos, j * 128 + c, window)) x[c] = -INFINITY;
+                    x[c] = key_visible(qpos, j * 128 + c, window) ? x[c] : -INFINITY;
                     m4[c & 3] = fmaxf(m4[c & 3], x[c]);
                 }
             } else {
