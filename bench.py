@@ -282,6 +282,37 @@ def bench_prefill(A, synth, kind: str, steps: int, warmup: int, world: int, stre
     return ms, prefill_flop(T, window)
 
 
+PACKED_SEQS, PACKED_LO, PACKED_HI = 16, 256, 16384
+
+
+def bench_prefill_packed(A, synth, steps: int, warmup: int, world: int, stream, seed: int):
+    """SWA prefill of a packed serving batch: 16 prompts with log-uniform
+    lengths in [256, 16384] (seeded), two rotating input sets larger than L2.
+    Returns ms per call, unmasked FLOP and the Q+K+V+O bytes of one call."""
+    import torch
+    lens = synth.packed_lengths(PACKED_SEQS, PACKED_LO, PACKED_HI, 1006)
+    sets = []
+    for s in range(2):
+        q, k, v, sink, cu = synth.packed_inputs(lens, HQ, HKV, D, seed + s, device="cuda")
+        sets.append((q, k, v, sink, torch.from_numpy(cu).cuda(), torch.empty_like(q)))
+    mx = int(lens.max())
+
+    def step(i):
+        q, k, v, sink, cu, o = sets[i % 2]
+        A.attn_swa_sink_prefill_varlen(q, k, v, cu, sink, window=W, max_seqlen=mx, out=o,
+                                       stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+        ms = time_region(step, steps, world, stream)
+    if A.attn_check_device_error(stream) != 0:
+        raise RuntimeError("packed prefill reported a device error")
+    flop = sum(4.0 * D * HQ * visible_pairs(int(n), W) for n in lens)
+    nbytes = 2.0 * float(lens.sum()) * (2 * HQ * D + 2 * HKV * D)
+    return ms, flop, nbytes, lens
+
+
 def bench_prefill_e2e(A, synth, steps: int, warmup: int, world: int, stream, seed: int):
     """Same metric through the public call with host buffers: every step
     copies its inputs (q, k, v, sink) from pinned host memory and its output
@@ -492,6 +523,16 @@ def main():
                                                          "peak": tf_burst, "unit": "TFLOP/s",
                                                          "frac": flop_ga / (ms_ga * 1e-3) / 1e12 / tf_burst,
                                                          "frac_sustained": flop_ga / (ms_ga * 1e-3) / 1e12 / tf_sus}}
+        ms_pk, flop_pk, bytes_pk, lens_pk = bench_prefill_packed(A, synth, steps_p, warmup, world,
+                                                                 stream, 1007 + 10 * rank)
+        parts["swa_prefill_packed_16seq"] = {
+            "config": f"{PACKED_SEQS} packed prompts, lengths log-uniform in "
+                      f"[{PACKED_LO}, {PACKED_HI}] (total {int(lens_pk.sum())} tokens), "
+                      "Hq=64 Hkv=8 D=128 W=128 bf16, cu_seqlens",
+            "value": flop_pk / (ms_pk * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms_pk,
+            "roofline": {"bound": "hbm", "achieved": bytes_pk / (ms_pk * 1e-3) / 1e9,
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": bytes_pk / (ms_pk * 1e-3) / 1e9 / hbm}}
         ctx4 = synth.context_lengths(64, 4096, 65536, 1004)
         ms4, kv4 = bench_verify_ga(A, ctx4, np.full(64, QMAX, np.int32), args.steps, warmup, world,
                                    stream, 1004 + 10 * rank)

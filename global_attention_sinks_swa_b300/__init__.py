@@ -37,6 +37,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_FAULT = range(5)
 ATTN_BF16, ATTN_F32 = 0, 1
 DEVERR_PAGE_OOB, DEVERR_CTX_OOB, DEVERR_QLEN, DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEVERR_SEQLENS = 0x10
 
 _vp, _ci, _cf, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -45,6 +46,8 @@ _SIGS = {
     "attn_check_device_error": ([_vp, ctypes.POINTER(ctypes.c_uint)], _ci),
     "attn_swa_sink_prefill": ([_vp] * 6 + [_ci] * 6 + [_cf, _ci, _vp], _ci),
     "attn_ga_sink_prefill": ([_vp] * 6 + [_ci] * 5 + [_cf, _ci, _vp], _ci),
+    "attn_swa_sink_prefill_varlen": ([_vp] * 7 + [_ci] * 7 + [_cf, _cf, _ci, _vp], _ci),
+    "attn_ga_sink_prefill_varlen": ([_vp] * 7 + [_ci] * 6 + [_cf, _cf, _ci, _vp], _ci),
     "attn_swa_ring_append": ([_vp] * 6 + [_ci] * 6 + [_vp], _ci),
     "attn_ga_paged_append": ([_vp] * 7 + [_ci] * 8 + [_vp], _ci),
     "attn_swa_sink_verify": ([_vp] * 7 + [_ci] * 7 + [_cf, _ci, _vp], _ci),
@@ -146,6 +149,54 @@ def attn_ga_sink_prefill(q, k, v, sink, scale: float | None = None, out=None, ls
                          stream=None):
     """Global (full causal) sink attention over whole sequences."""
     return _prefill(False, q, k, v, sink, 0, scale, out, lse, stream)
+
+
+def _prefill_varlen(swa: bool, q, k, v, cu_seqlens, sink, window, max_seqlen, scale,
+                    value_scale, out, lse, stream):
+    _cuda(q, k, v, cu_seqlens, sink, out, lse)
+    total, Hq, D = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.shape[0] - 1
+    if k.shape != (total, Hkv, D) or v.shape != k.shape or sink.shape != (Hq,) or B < 0:
+        raise ValueError("shapes: q [total,Hq,D], k/v [total,Hkv,D], cu_seqlens [B+1], sink [Hq]")
+    if k.dtype != q.dtype or v.dtype != q.dtype or sink.dtype != torch.float32:
+        raise TypeError("q/k/v share one dtype; sink is float32")
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens is int32")
+    if max_seqlen is None:  # one device-to-host read; pass it to stay asynchronous
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if B > 0 else 0
+    out = torch.empty_like(q) if out is None else out
+    if lse is not None and (lse.shape != (Hq, total) or lse.dtype != torch.float32):
+        raise ValueError("lse must be float32 [Hq,total]")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(sink), _ptr(out), _ptr(lse), B,
+            total, int(max_seqlen), Hq, Hkv, D]
+    if swa:
+        st = _lib.attn_swa_sink_prefill_varlen(*args, int(window), scale, float(value_scale),
+                                               _dtype_code(q), _stream(stream))
+    else:
+        st = _lib.attn_ga_sink_prefill_varlen(*args, scale, float(value_scale), _dtype_code(q),
+                                              _stream(stream))
+    _check(st)
+    return out
+
+
+def attn_swa_sink_prefill_varlen(q, k, v, cu_seqlens, sink, window: int = 128,
+                                 max_seqlen: int | None = None, scale: float | None = None,
+                                 value_scale: float = 1.0, out=None, lse=None, stream=None):
+    """Sliding-window sink attention over a packed batch of sequences.
+    q [total,Hq,D], k/v [total,Hkv,D], cu_seqlens [B+1] int32 (device),
+    sink [Hq] fp32 -> o [total,Hq,D] = value_scale * attention; lse [Hq,total]."""
+    return _prefill_varlen(True, q, k, v, cu_seqlens, sink, window, max_seqlen, scale,
+                           value_scale, out, lse, stream)
+
+
+def attn_ga_sink_prefill_varlen(q, k, v, cu_seqlens, sink, max_seqlen: int | None = None,
+                                scale: float | None = None, value_scale: float = 1.0, out=None,
+                                lse=None, stream=None):
+    """Global (full causal) sink attention over a packed batch of sequences."""
+    return _prefill_varlen(False, q, k, v, cu_seqlens, sink, 0, max_seqlen, scale, value_scale,
+                           out, lse, stream)
 
 
 def _append_common(k_new, v_new, cu_q, seq_lens, kc, vc):

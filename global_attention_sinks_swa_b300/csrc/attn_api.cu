@@ -12,6 +12,8 @@
 #include "index_math.cuh"
 #include "internal.h"
 
+#include <cmath>
+
 #define ATTN_EXPORT extern "C" __attribute__((visibility("default")))
 
 namespace {
@@ -87,13 +89,14 @@ bool make_map_4d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, const
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// [rows, H, 128] bf16 tensor viewed as (128, H, rows) with a box of (64, bh, 1).
-bool map_3d(CUtensorMap *m, const void *base, uint64_t rows, int H, uint32_t bh) {
+// [rows, H, 128] bf16 tensor viewed as (128, H, rows) with a box of (64, bh, bt).
+bool map_3d(CUtensorMap *m, const void *base, uint64_t rows, int H, uint32_t bh,
+            uint32_t bt = 1) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t gd[3] = {128, static_cast<cuuint64_t>(H), rows};
     cuuint64_t gs[2] = {256, static_cast<cuuint64_t>(H) * 256};
-    cuuint32_t bx[3] = {64, bh, 1};
+    cuuint32_t bx[3] = {64, bh, bt};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), gd, gs, bx, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -103,63 +106,59 @@ bool map_3d(CUtensorMap *m, const void *base, uint64_t rows, int H, uint32_t bh)
 
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
-// [B,T,H,D] bf16 tensor viewed as (D, H, T, B) with a box of (64, bh, bt, 1).
-bool map_bthd(CUtensorMap *m, const void *base, int B, int T, int H, uint32_t bh, uint32_t bt) {
-    const uint64_t D = 128;
-    uint64_t dims[4] = {D, static_cast<uint64_t>(H), static_cast<uint64_t>(T),
-                        static_cast<uint64_t>(B)};
-    uint64_t strides[3] = {D * 2, static_cast<uint64_t>(H) * D * 2,
-                           static_cast<uint64_t>(T) * H * D * 2};
-    uint32_t box[4] = {64, bh, bt, 1};
-    return make_map_4d(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, strides, box);
-}
-
-attn_status_t prefill_common(const void *q, const void *k, const void *v, const float *sink,
-                             void *o, float *lse, int B, int T, int Hq, int Hkv, int D, int window,
-                             float scale, attn_dtype_t dtype, void *stream, bool swa) {
+// Both prefill entry points, batches of equal length (cu == nullptr, total =
+// B*T) and packed batches (cu[B+1] on the device, T = the longest sequence).
+attn_status_t prefill_common(const void *q, const void *k, const void *v, const int32_t *cu,
+                             const float *sink, void *o, float *lse, int B, int T, long total,
+                             int Hq, int Hkv, int D, int window, float scale, float vscale,
+                             attn_dtype_t dtype, void *stream, bool swa) {
     if (!q || !k || !v || !sink || !o) return fail(ATTN_ERR_INVALID_ARG, "null pointer argument");
-    if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0)
-        return fail(ATTN_ERR_INVALID_ARG, "bad sizes B=%d T=%d Hq=%d Hkv=%d D=%d", B, T, Hq, Hkv, D);
+    if (B < 0 || T < 0 || total < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "bad sizes B=%d T=%d total=%ld Hq=%d Hkv=%d D=%d", B, T,
+                    total, Hq, Hkv, D);
     if (swa && window < 1) return fail(ATTN_ERR_INVALID_ARG, "window must be >= 1 (got %d)", window);
     if (!(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "scale must be > 0");
+    if (!std::isfinite(vscale)) return fail(ATTN_ERR_INVALID_ARG, "value_scale must be finite");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return fail(ATTN_ERR_INVALID_ARG, "q/k/v/o must be 16-byte aligned");
-    if (static_cast<long long>(B) * T * Hq >= (1ll << 31))
-        return fail(ATTN_ERR_UNSUPPORTED, "B*T*Hq must be < 2^31");
+    if (total * Hq >= (1ll << 31)) return fail(ATTN_ERR_UNSUPPORTED, "tokens*Hq must be < 2^31");
     unsigned *err = device_error_word();
     if (!err) return fail(ATTN_ERR_CUDA, "no CUDA device / error word unavailable");
     cudaStream_t s = as_stream(stream);
     const int win = swa ? window : 0;
+    const attn::PrefillBatch pb{cu, B, T, static_cast<int>(total)};
     if (dtype == ATTN_F32) {
         if (D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "fp32 prefill needs D in {64,128}");
+        if (B == 0 || total == 0) return ok();
         cudaError_t e = attn::launch_prefill_f32(
             static_cast<const float *>(q), static_cast<const float *>(k),
-            static_cast<const float *>(v), sink, static_cast<float *>(o), lse, B, T, Hq, Hkv, D,
-            win, scale, err, s);
+            static_cast<const float *>(v), sink, static_cast<float *>(o), lse, pb, Hq, Hkv, D, win,
+            scale, vscale, err, s);
         return e == cudaSuccess ? ok() : cuda_fail(e, "prefill_f32 launch");
     }
     if (dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "bf16 prefill needs D = 128 (got %d)", D);
-    if (B == 0 || T == 0) return ok();
+    if (B == 0 || total == 0 || T == 0) return ok();
     const int G = Hq / Hkv;
     attn::PrefillMaps maps;
     maps.out = o;
+    const uint64_t rows = static_cast<uint64_t>(total);
     const bool packed = swa && attn::prefill_swa_tc_supported(G, window);
     bool good;
     if (packed) {  // Q tiles of 16 tokens x 8 heads; K/V in 16-key ring blocks
         const uint32_t TT = static_cast<uint32_t>(attn::kSwaTokens);
         const uint32_t NB = static_cast<uint32_t>(attn::kSwaBlockKeys);
-        good = map_bthd(&maps.q, q, B, T, Hq, G, TT) && map_bthd(&maps.k, k, B, T, Hkv, 1, NB) &&
-               map_bthd(&maps.v, v, B, T, Hkv, 1, NB);
+        good = map_3d(&maps.q, q, rows, Hq, G, TT) && map_3d(&maps.k, k, rows, Hkv, 1, NB) &&
+               map_3d(&maps.v, v, rows, Hkv, 1, NB);
     } else {
-        good = map_bthd(&maps.q, q, B, T, Hq, 1, 128) && map_bthd(&maps.k, k, B, T, Hkv, 1, 128) &&
-               map_bthd(&maps.v, v, B, T, Hkv, 1, 128) && map_bthd(&maps.o, o, B, T, Hq, 1, 128);
+        good = map_3d(&maps.q, q, rows, Hq, 1, 128) && map_3d(&maps.k, k, rows, Hkv, 1, 128) &&
+               map_3d(&maps.v, v, rows, Hkv, 1, 128) && map_3d(&maps.o, o, rows, Hq, 1, 128);
     }
     if (!good) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the prefill maps");
-    cudaError_t e = packed ? attn::launch_prefill_swa_tc(maps, sink, lse, B, T, Hq, Hkv, window,
-                                                         scale, err, s)
-                           : attn::launch_prefill_ga_tc(maps, sink, lse, B, T, Hq, Hkv, win, scale,
-                                                        err, s);
+    cudaError_t e = packed ? attn::launch_prefill_swa_tc(maps, sink, lse, pb, Hq, Hkv, window,
+                                                         scale, vscale, err, s)
+                           : attn::launch_prefill_ga_tc(maps, sink, lse, pb, Hq, Hkv, win, scale,
+                                                        vscale, err, s);
     return e == cudaSuccess ? ok() : cuda_fail(e, "prefill launch");
 }
 
@@ -223,15 +222,34 @@ ATTN_EXPORT attn_status_t attn_swa_sink_prefill(const void *q, const void *k, co
                                                 const float *sink, void *o, float *lse, int B,
                                                 int T, int Hq, int Hkv, int D, int window,
                                                 float scale, attn_dtype_t dtype, void *stream) {
-    return prefill_common(q, k, v, sink, o, lse, B, T, Hq, Hkv, D, window, scale, dtype, stream,
-                          true);
+    return prefill_common(q, k, v, nullptr, sink, o, lse, B, T, static_cast<long>(B) * T, Hq, Hkv,
+                          D, window, scale, 1.f, dtype, stream, true);
 }
 
 ATTN_EXPORT attn_status_t attn_ga_sink_prefill(const void *q, const void *k, const void *v,
                                                const float *sink, void *o, float *lse, int B, int T,
                                                int Hq, int Hkv, int D, float scale,
                                                attn_dtype_t dtype, void *stream) {
-    return prefill_common(q, k, v, sink, o, lse, B, T, Hq, Hkv, D, 0, scale, dtype, stream, false);
+    return prefill_common(q, k, v, nullptr, sink, o, lse, B, T, static_cast<long>(B) * T, Hq, Hkv,
+                          D, 0, scale, 1.f, dtype, stream, false);
+}
+
+ATTN_EXPORT attn_status_t attn_swa_sink_prefill_varlen(
+    const void *q, const void *k, const void *v, const int32_t *cu_seqlens, const float *sink,
+    void *o, float *lse, int B, int total_tokens, int max_seqlen, int Hq, int Hkv, int D,
+    int window, float scale, float value_scale, attn_dtype_t dtype, void *stream) {
+    if (!cu_seqlens) return fail(ATTN_ERR_INVALID_ARG, "null pointer argument");
+    return prefill_common(q, k, v, cu_seqlens, sink, o, lse, B, max_seqlen, total_tokens, Hq, Hkv,
+                          D, window, scale, value_scale, dtype, stream, true);
+}
+
+ATTN_EXPORT attn_status_t attn_ga_sink_prefill_varlen(
+    const void *q, const void *k, const void *v, const int32_t *cu_seqlens, const float *sink,
+    void *o, float *lse, int B, int total_tokens, int max_seqlen, int Hq, int Hkv, int D,
+    float scale, float value_scale, attn_dtype_t dtype, void *stream) {
+    if (!cu_seqlens) return fail(ATTN_ERR_INVALID_ARG, "null pointer argument");
+    return prefill_common(q, k, v, cu_seqlens, sink, o, lse, B, max_seqlen, total_tokens, Hq, Hkv,
+                          D, 0, scale, value_scale, dtype, stream, false);
 }
 
 ATTN_EXPORT attn_status_t attn_swa_ring_append(const void *k_new, const void *v_new,
@@ -444,7 +462,8 @@ ATTN_EXPORT attn_status_t attn_debug_swa_stream_visits(int32_t *visits, int B, i
         return fail(ATTN_ERR_INVALID_ARG, "bad arguments");
     if (!attn::prefill_swa_tc_supported(attn::kSwaHeads, window))
         return fail(ATTN_ERR_UNSUPPORTED, "the streaming SWA kernel needs a window in [114, 129]");
-    if (grid == 0 && B > 0 && T > 0) grid = attn::prefill_swa_grid(B, T, Hkv);
+    if (grid == 0 && B > 0 && T > 0)
+        grid = attn::prefill_swa_grid(static_cast<long>(B) * Hkv * attn::swa_seq_blocks(T));
     cudaError_t e = attn::launch_debug_swa_stream_visits(visits, B, T, Hkv, window, grid,
                                                          as_stream(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "debug swa stream visits");

@@ -49,23 +49,27 @@ __global__ void swa_stream_visits_kernel(int32_t *visits, int B, int T, int Hkv,
                                          int grid) {
     const int cta = blockIdx.x * blockDim.x + threadIdx.x;
     if (cta >= grid) return;
-    const int nblk = (T + kSwaTokens - 1) / kSwaTokens;
-    const int ntiles = nblk * Hkv * B;
+    const int32_t *cu = nullptr;  // equal lengths (the packed order is replayed on the host)
+    const int total = B * T;
+    const int ntiles = swa_total_tiles(cu, B, T, total, Hkv);
     int u0, u1;
     swa_stream_range(cta, grid, ntiles, &u0, &u1);
+    if (u0 >= u1) return;
     SwaRingCursor cur;
+    SwaTileCursor t = swa_cursor_at(cu, B, T, total, Hkv, u0);
     int slot_key[kSwaRingBlocks];
     for (int s = 0; s < kSwaRingBlocks; ++s) slot_key[s] = -(1 << 30);
     for (int u = u0; u < u1; ++u) {
-        const int bg = u / nblk, i0 = (u - bg * nblk) * kSwaTokens;
+        if (u > u0) swa_cursor_next(t, cu, B, T, total, Hkv);
+        const int bg = t.b * Hkv + t.g, i0 = t.blk * kSwaTokens;
         const int key0 = i0 + kSwaTokens - kSwaKeys;
         swa_ring_step(cur, bg, kSwaTileBlocks);
         for (int s = cur.first_new; s < cur.first_new + cur.n_new; ++s)
             slot_key[s % kSwaRingBlocks] = key0 + kSwaBlockKeys * (s - cur.base);
         const bool interior = key0 >= 0;
-        for (int t = 0; t < kSwaTokens; ++t) {
-            const int qpos = i0 + t;
-            if (qpos >= T) break;
+        for (int tt = 0; tt < kSwaTokens; ++tt) {
+            const int qpos = i0 + tt;
+            if (qpos >= t.len) break;
             int c_lo, c_hi;
             swa_row_cols(qpos, key0, window, &c_lo, &c_hi);
             int32_t *row = visits + (static_cast<long>(bg) * T + qpos) * (T + 1);
@@ -74,7 +78,7 @@ __global__ void swa_stream_visits_kernel(int32_t *visits, int B, int T, int Hkv,
                 for (int cc = 0; cc < kSwaBlockKeys; ++cc) {
                     if (!swa_col_admitted(j * kSwaBlockKeys + cc, c_lo, c_hi, interior)) continue;
                     const int key = kb + cc;
-                    atomicAdd(&row[(key >= 0 && key < T) ? key : T], 1);
+                    atomicAdd(&row[(key >= 0 && key < t.len) ? key : T], 1);
                 }
             }
         }

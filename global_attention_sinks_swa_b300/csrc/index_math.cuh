@@ -62,6 +62,38 @@ ATTN_HD RingVisible ring_visible_slots(int L, int R, int window, int qpos) {
     return v;
 }
 
+// ---- prefill batches: sequence b covers the tokens [start, start + len) of
+// the flattened token axis.  cu == nullptr: B sequences of T tokens each
+// (start = b*T); otherwise the packed layout cu[b] .. cu[b+1] with
+// cu[B] = total and T >= every length.  A span outside [0, total), longer
+// than T or with a negative length is invalid: it holds no tokens and the
+// kernels report it.
+struct SeqSpan {
+    int start, len;
+    bool ok;
+};
+ATTN_HD SeqSpan seq_span(const int32_t *cu, int b, int T, int total) {
+    SeqSpan s;
+    if (!cu) {
+        s.start = b * T;
+        s.len = T;
+        s.ok = true;
+        return s;
+    }
+    s.start = cu[b];
+    const int e = cu[b + 1];
+    s.ok = (s.start >= 0) & (e >= s.start) & (e <= total) & (e - s.start <= T);
+    s.len = s.ok ? e - s.start : 0;
+    return s;
+}
+// Index of the LSE of (sequence b, head h, position i): [B, Hq, T] for
+// batches of equal length, [Hq, total] for packed batches.
+ATTN_HD long lse_index(const int32_t *cu, int b, int h, int i, int start, int T, int total,
+                       int Hq) {
+    return cu ? static_cast<long>(h) * total + start + i
+              : (static_cast<long>(b) * Hq + h) * T + i;
+}
+
 // ---- GA prefill tiling: BM query rows per tile, BN keys per key tile.
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
@@ -101,7 +133,7 @@ ATTN_HD int swa_pack_key0(int i0, int G, int window) {
 }
 
 // ---- streaming SWA prefill (G = 8, 16 tokens x 8 heads per tile, N = 144):
-// a CTA walks a contiguous run of tiles in the order u = (b*Hkv + g)*nblk + blk
+// a CTA walks a contiguous run of tiles in (b, g, token block) order
 // and keeps the keys of the current window in a ring of 16-key blocks in
 // shared memory, so each tile loads one new K/V block (nine after a change of
 // (b, g) or at the start of the run).
@@ -116,6 +148,53 @@ constexpr int kSwaRingBlocks = 12;                // ring capacity in blocks
 ATTN_HD void swa_stream_range(int cta, int grid, int ntiles, int *u0, int *u1) {
     *u0 = static_cast<int>((static_cast<long long>(cta) * ntiles) / grid);
     *u1 = static_cast<int>((static_cast<long long>(cta + 1) * ntiles) / grid);
+}
+
+// A tile of the streaming order: sequence b, kv head g, token block blk of
+// the nblk blocks of sequence b (tokens start + 16*blk ..).  Tiles run in
+// (b, g, blk) order over the sequences that hold tokens.
+struct SwaTileCursor {
+    int b, g, blk, nblk, start, len;
+};
+ATTN_HD int swa_seq_blocks(int len) { return (len + kSwaTokens - 1) / kSwaTokens; }
+ATTN_HD void swa_cursor_seq(SwaTileCursor &c, const int32_t *cu, int T, int total) {
+    const SeqSpan s = seq_span(cu, c.b, T, total);
+    c.start = s.start;
+    c.len = s.len;
+    c.nblk = swa_seq_blocks(s.len);
+}
+// The next tile of the order (past the last tile: b == B).
+ATTN_HD void swa_cursor_next(SwaTileCursor &c, const int32_t *cu, int B, int T, int total,
+                             int Hkv) {
+    if (++c.blk < c.nblk) return;
+    c.blk = 0;
+    if (++c.g < Hkv) return;
+    c.g = 0;
+    while (++c.b < B) {
+        swa_cursor_seq(c, cu, T, total);
+        if (c.nblk > 0) return;
+    }
+}
+// Serial reference of the order: the number of tiles, and tile u.
+ATTN_HD int swa_total_tiles(const int32_t *cu, int B, int T, int total, int Hkv) {
+    int n = 0;
+    for (int b = 0; b < B; ++b) n += swa_seq_blocks(seq_span(cu, b, T, total).len) * Hkv;
+    return n;
+}
+ATTN_HD SwaTileCursor swa_cursor_at(const int32_t *cu, int B, int T, int total, int Hkv, int u) {
+    SwaTileCursor c;
+    c.g = c.blk = c.nblk = c.start = c.len = 0;
+    for (c.b = 0; c.b < B; ++c.b) {
+        swa_cursor_seq(c, cu, T, total);
+        const int nt = c.nblk * Hkv;
+        if (u < nt) {
+            c.g = u / c.nblk;
+            c.blk = u - c.g * c.nblk;
+            return c;
+        }
+        u -= nt;
+    }
+    return c;
 }
 
 // Block bookkeeping in load order: every block a CTA loads gets the next

@@ -8,10 +8,20 @@
 
 namespace attn {
 
-// fp32 CUDA-core prefill (window <= 0: global attention).
+// Sequences of a prefill batch: B sequences of T tokens each (cu == nullptr,
+// total = B*T), or B packed sequences given by the device array cu[B+1] with
+// cu[B] = total tokens and T >= the longest one (T sizes grids only).
+struct PrefillBatch {
+    const int32_t *cu;
+    int B, T, total;
+};
+
+// fp32 CUDA-core prefill (window <= 0: global attention).  The output is
+// multiplied by vscale.
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *sink,
-                               float *o, float *lse, int B, int T, int Hq, int Hkv, int D,
-                               int window, float scale, unsigned int *err, cudaStream_t s);
+                               float *o, float *lse, const PrefillBatch &pb, int Hq, int Hkv,
+                               int D, int window, float scale, float vscale, unsigned int *err,
+                               cudaStream_t s);
 
 // Tensor maps of a bf16 prefill problem (built by attn_api.cu).
 struct PrefillMaps {
@@ -22,17 +32,19 @@ struct PrefillMaps {
     void *out;      // output base pointer (kernels that store O without TMA)
 };
 
+// The prefill maps view Q, K, V and O as [total tokens, heads, D] (3-D).
 // tcgen05 GA-tiled prefill (full causal, or window-limited when window > 0).
-cudaError_t launch_prefill_ga_tc(const PrefillMaps &maps, const float *sink, float *lse, int B,
-                                 int T, int Hq, int Hkv, int window, float scale,
-                                 unsigned int *err, cudaStream_t s);
+cudaError_t launch_prefill_ga_tc(const PrefillMaps &maps, const float *sink, float *lse,
+                                 const PrefillBatch &pb, int Hq, int Hkv, int window, float scale,
+                                 float vscale, unsigned int *err, cudaStream_t s);
 // tcgen05 streaming SWA prefill (G = 8: 16 tokens x 8 heads per tile, window
 // in [114, 129]); one persistent CTA per SM over prefill_swa_grid() CTAs.
-cudaError_t launch_prefill_swa_tc(const PrefillMaps &maps, const float *sink, float *lse, int B,
-                                  int T, int Hq, int Hkv, int window, float scale,
-                                  unsigned int *err, cudaStream_t s);
+cudaError_t launch_prefill_swa_tc(const PrefillMaps &maps, const float *sink, float *lse,
+                                  const PrefillBatch &pb, int Hq, int Hkv, int window, float scale,
+                                  float vscale, unsigned int *err, cudaStream_t s);
 int prefill_swa_tc_supported(int G, int window);
-int prefill_swa_grid(int B, int T, int Hkv);
+// CTAs of the streaming kernel for a batch of at most max_tiles tiles.
+int prefill_swa_grid(long max_tiles);
 
 // KV-cache appends (plain 16-byte copies).
 cudaError_t launch_ring_append(const void *k_new, const void *v_new, const int32_t *cu_q,

@@ -1,10 +1,11 @@
 // fp32 sink-attention prefill on CUDA cores (FFMA, no TF32): the fp32-I/O path
-// of attn_{swa,ga}_sink_prefill.  One warp computes one (b, i, h) output row
+// of attn_{swa,ga}_sink_prefill{,_varlen}.  One warp computes one output row
 // with an online softmax whose running max starts at the sink logit and whose
 // running sum starts at the sink's own term (technical-report summary,
 // section "Hybrid Sliding Window Attention Architecture": learnable sink bias;
 // the sink adds to the denominator only).  Keys are the causal window
 // (section "MiMo-V2-Flash Model Architecture": W = 128) or the full prefix.
+#include "attn_sink.h"
 #include "index_math.cuh"
 #include "internal.h"
 #include "ptx_sm103.cuh"
@@ -19,32 +20,51 @@ template <int D>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                        const float *__restrict__ v, const float *__restrict__ sink,
-                       float *__restrict__ o, float *__restrict__ lse, int B, int T, int Hq,
-                       int Hkv, int window, float scale) {
+                       float *__restrict__ o, float *__restrict__ lse,
+                       const int32_t *__restrict__ cu, int B, int T, int total, int Hq, int Hkv,
+                       int window, float scale, float vscale, unsigned *err) {
     constexpr int E = D / 32;  // elements per lane
     const int lane = threadIdx.x & 31;
     const long row = static_cast<long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-    const long nrows = static_cast<long>(B) * T * Hq;
+    const long nrows = static_cast<long>(total) * Hq;
     if (row >= nrows) return;
-    // rows are ordered (b, h, i) so that the warps of a block share keys
-    const int i = static_cast<int>(row % T);
-    const int h = static_cast<int>((row / T) % Hq);
-    const int b = static_cast<int>(row / (static_cast<long>(T) * Hq));
+    // rows are ordered (h, token) so that the warps of a block share keys
+    const int tok = static_cast<int>(row % total);
+    const int h = static_cast<int>(row / total);
+    int b;
+    if (!cu) {
+        b = tok / T;
+    } else {  // the last sequence starting at or before tok
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cu[mid] <= tok) lo = mid;
+            else hi = mid - 1;
+        }
+        b = lo;
+    }
+    const SeqSpan span = seq_span(cu, b, T, total);
+    if (!span.ok) {
+        if (lane == 0 && h == 0) atomicOr(err, ATTN_DEVERR_SEQLENS);
+        return;
+    }
+    const int i = tok - span.start;
+    if (i < 0 || i >= span.len) return;  // a token outside every valid sequence
     const int g = h / (Hq / Hkv);
 
-    const float *qrow = q + ((static_cast<long>(b) * T + i) * Hq + h) * D;
+    const float *qrow = q + (static_cast<long>(tok) * Hq + h) * D;
     float qv[E], acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         qv[e] = qrow[lane + 32 * e] * (scale * kLog2e);  // scores in log2 units
         acc[e] = 0.f;
     }
-    float *orow = o + ((static_cast<long>(b) * T + i) * Hq + h) * D;
+    float *orow = o + (static_cast<long>(tok) * Hq + h) * D;
     const float sig = sink[h];
     if (isinf(sig) && sig > 0.f) {  // the sink takes all the probability mass
 #pragma unroll
         for (int e = 0; e < E; ++e) orow[lane + 32 * e] = 0.f;
-        if (lse && lane == 0) lse[(static_cast<long>(b) * Hq + h) * T + i] = INFINITY;
+        if (lse && lane == 0) lse[lse_index(cu, b, h, i, span.start, T, total, Hq)] = INFINITY;
         return;
     }
     float m = sig * kLog2e;                   // running max (log2 units)
@@ -52,8 +72,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     int lo = 0;
     if (window > 0) lo = max(0, i - window + 1);
     const long kstride = static_cast<long>(Hkv) * D;
-    const float *kb = k + (static_cast<long>(b) * T * Hkv + g) * D;
-    const float *vb = v + (static_cast<long>(b) * T * Hkv + g) * D;
+    const float *kb = k + (static_cast<long>(span.start) * Hkv + g) * D;
+    const float *vb = v + (static_cast<long>(span.start) * Hkv + g) * D;
     for (int j = lo; j <= i; ++j) {
         if (!key_visible(i, j, window)) continue;
         const float *kr = kb + j * kstride;
@@ -71,28 +91,30 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], alpha, p * vr[lane + 32 * e]);
         m = mn;
     }
-    const float inv = 1.f / l;
+    const float inv = vscale / l;  // the value scale rides on 1/l
 #pragma unroll
     for (int e = 0; e < E; ++e) orow[lane + 32 * e] = acc[e] * inv;
     if (lse && lane == 0)
-        lse[(static_cast<long>(b) * Hq + h) * T + i] = (m + log2f(l)) * 0.6931471805599453f;
+        lse[lse_index(cu, b, h, i, span.start, T, total, Hq)] = (m + log2f(l)) * 0.6931471805599453f;
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *sink,
-                               float *o, float *lse, int B, int T, int Hq, int Hkv, int D,
-                               int window, float scale, unsigned int * /*err*/, cudaStream_t s) {
-    const long nrows = static_cast<long>(B) * T * Hq;
+                               float *o, float *lse, const PrefillBatch &pb, int Hq, int Hkv,
+                               int D, int window, float scale, float vscale, unsigned int *err,
+                               cudaStream_t s) {
+    if (pb.B == 0) return cudaSuccess;
+    const long nrows = static_cast<long>(pb.total) * Hq;
     if (nrows == 0) return cudaSuccess;
     dim3 grid(static_cast<unsigned>((nrows + kWarpsPerBlock - 1) / kWarpsPerBlock));
     dim3 block(kWarpsPerBlock * 32);
     if (D == 64)
-        prefill_f32_kernel<64><<<grid, block, 0, s>>>(q, k, v, sink, o, lse, B, T, Hq, Hkv, window,
-                                                     scale);
+        prefill_f32_kernel<64><<<grid, block, 0, s>>>(q, k, v, sink, o, lse, pb.cu, pb.B, pb.T,
+                                                     pb.total, Hq, Hkv, window, scale, vscale, err);
     else
-        prefill_f32_kernel<128><<<grid, block, 0, s>>>(q, k, v, sink, o, lse, B, T, Hq, Hkv,
-                                                      window, scale);
+        prefill_f32_kernel<128><<<grid, block, 0, s>>>(q, k, v, sink, o, lse, pb.cu, pb.B, pb.T,
+                                                      pb.total, Hq, Hkv, window, scale, vscale, err);
     return cudaGetLastError();
 }
 

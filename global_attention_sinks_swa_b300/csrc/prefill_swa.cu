@@ -9,7 +9,10 @@
 //
 // Tiling: a tile is 16 consecutive tokens x the 8 query heads that share one
 // kv head (GQA packing, row r = 8*t + hh), i.e. 128 rows, against the 144 keys
-// key0 = i0 - 128 .. i0 + 15 that cover every key its rows can see.  Each
+// key0 = i0 - 128 .. i0 + 15 that cover every key its rows can see.  A batch
+// is B sequences, of T tokens each or packed by cu_seqlens; every sequence
+// starts its own tile grid at its first token (positions are relative to the
+// sequence, and keys before it are masked like keys before position 0).  Each
 // persistent CTA walks a contiguous run of tiles in (b, g, token block) order
 // (swa_stream_range), so consecutive tiles share 128 of their 144 keys: K and
 // V live in a ring of 16-key blocks in shared memory and a tile loads one new
@@ -70,32 +73,81 @@ struct __align__(1024) Smem {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
+    SwaTileCursor first;  // the CTA's first tile
+    int ntile;            // and the number of tiles in its run
 };
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory of one CTA");
 
-// Tile u of the linear order: batch, kv head and first token.
-struct Tile {
-    int b, g, i0, bg;
-};
-ATTN_DEV Tile tile_at(int u, int nblk, int Hkv) {
-    Tile t;
-    t.bg = u / nblk;
-    t.i0 = (u - t.bg * nblk) * kTT;
-    t.g = t.bg % Hkv;
-    t.b = t.bg / Hkv;
-    return t;
+// Warp-cooperative forms of the tile order (swa_total_tiles and
+// swa_cursor_at; every lane returns the same): the number of tiles of the
+// batch, with *bad set when a packed span is invalid, and the cursor of tile u.
+ATTN_DEV int count_tiles_warp(const int32_t *cu, int B, int T, int total, int Hkv, int lane,
+                              bool *bad) {
+    *bad = false;
+    if (!cu) return B * Hkv * swa_seq_blocks(T);
+    int n = 0;
+    bool ok = true;
+    for (int b = lane; b < B; b += 32) {
+        const SeqSpan sp = seq_span(cu, b, T, total);
+        n += swa_seq_blocks(sp.len) * Hkv;
+        ok &= sp.ok;
+    }
+    for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    *bad = !__all_sync(0xffffffffu, ok);
+    return n;
+}
+ATTN_DEV SwaTileCursor cursor_at_warp(const int32_t *cu, int B, int T, int total, int Hkv, int u,
+                                      int lane) {
+    SwaTileCursor c;
+    c.g = c.blk = 0;
+    if (!cu) {
+        c.nblk = swa_seq_blocks(T);
+        const int bg = u / c.nblk;
+        c.blk = u - bg * c.nblk;
+        c.b = bg / Hkv;
+        c.g = bg - c.b * Hkv;
+        c.start = c.b * T;
+        c.len = T;
+        return c;
+    }
+    int acc = 0;  // tiles of the sequences before this chunk of 32
+    for (int c0 = 0; c0 < B; c0 += 32) {
+        const int b = c0 + lane;
+        const int nt = b < B ? swa_seq_blocks(seq_span(cu, b, T, total).len) * Hkv : 0;
+        int incl = nt;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, acc + incl > u);
+        if (hit) {  // the first such lane holds tile u (and has tiles)
+            const int src = __ffs(static_cast<int>(hit)) - 1;
+            const int excl = __shfl_sync(0xffffffffu, incl - nt, src);
+            c.b = c0 + src;
+            swa_cursor_seq(c, cu, T, total);
+            const int rem = u - acc - excl;
+            c.g = rem / c.nblk;
+            c.blk = rem - c.g * c.nblk;
+            return c;
+        }
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    c.b = B;
+    c.nblk = c.start = c.len = 0;
+    return c;
 }
 
-// Per-tile state of the MMA issuer: the tile's ring blocks and the blocks it
-// releases after use.
+// Per-tile state of the MMA issuer: the tile, its ring blocks and the blocks
+// it releases after use.
 struct Issue {
     SwaRingCursor cur;
+    SwaTileCursor t;      // the tile
     int k = 0;            // tile index within the CTA's run
     int rel_end = 0;      // blocks [cur.base, rel_end) are released after this tile
     int waited = -1;      // highest block sequence number whose full barrier was seen
-    __device__ void advance(int u0, int n, int nblk) {
-        const int bg = (u0 + k) / nblk;
-        swa_ring_step(cur, bg, kNB);
-        const bool next_same = (k + 1 < n) && ((u0 + k + 1) / nblk == bg);
+    __device__ void advance(int n, int Hkv) {
+        swa_ring_step(cur, t.b * Hkv + t.g, kNB);
+        const bool next_same = (k + 1 < n) && (t.blk + 1 < t.nblk);
         rel_end = swa_ring_release_end(cur.base, next_same, kNB);
     }
 };
@@ -115,17 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                               const __grid_constant__ CUtensorMap tmk,
                               const __grid_constant__ CUtensorMap tmv,
                               __nv_bfloat16 *__restrict__ out, const float *__restrict__ sink,
-                              float *__restrict__ lse, int B, int T, int Hq, int Hkv, int window,
-                              float scale, unsigned *err) {
+                              float *__restrict__ lse, const int32_t *__restrict__ cu, int B,
+                              int T, int total, int Hq, int Hkv, int window, float scale,
+                              float vscale, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nblk = (T + kTT - 1) / kTT;
-    const int ntiles = nblk * Hkv * B;
-    int u0, u1;
-    swa_stream_range(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), ntiles, &u0, &u1);
-    const int n = u1 - u0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kQStages; ++s) {
@@ -148,6 +196,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.abort = ptx::prior_timeout(err) ? 1 : 0;
         ptx::fence_mbar_init();
     }
+    if (warp == 0) {  // this CTA's run of tiles
+        bool bad;
+        const int ntiles = count_tiles_warp(cu, B, T, total, Hkv, lane, &bad);
+        int u0, u1;
+        swa_stream_range(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), ntiles, &u0,
+                         &u1);
+        SwaTileCursor c;
+        c.b = B;
+        c.g = c.blk = c.nblk = c.start = c.len = 0;
+        if (u0 < u1) c = cursor_at_warp(cu, B, T, total, Hkv, u0, lane);
+        if (lane == 0) {
+            sm.first = c;
+            sm.ntile = u1 - u0;
+            if (bad && blockIdx.x == 0) atomicOr(err, kErrSeqlens);
+        }
+    }
     if (warp == 9) {
         ptx::tmem_alloc(&sm.tmem_base, 512);
         ptx::tmem_relinquish();
@@ -157,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const bool skip = sm.abort != 0;  // an earlier launch timed out: do nothing
+    const int n = sm.ntile;
+    const SwaTileCursor first = sm.first;
 
     if (warp == 8 || warp == 10) {
         // --------------------------------------------- TMA producers
@@ -173,12 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *ring = qk ? sm.k[0] : sm.v[0];
             const CUtensorMap *map = qk ? &tmk : &tmv;
             SwaRingCursor cur;
+            SwaTileCursor t = first;
             bool ok = true;
             int last_q = -1, last_s = -1;  // last Q tile and ring block issued
             for (int k = 0; ok && k < n; ++k) {
-                const Tile t = tile_at(u0 + k, nblk, Hkv);
-                const int key0 = t.i0 + kTT - kN;
-                swa_ring_step(cur, t.bg, kNB);
+                if (k > 0) swa_cursor_next(t, cu, B, T, total, Hkv);
+                const int i0 = t.blk * kTT;
+                const int key0 = i0 + kTT - kN;
+                swa_ring_step(cur, t.b * Hkv + t.g, kNB);
                 if (qk) {
                     const int st = k % kQStages;
                     if (k >= kQStages && !ptx::mbar_wait(&sm.q_empty[st], ((k / kQStages) - 1) & 1)) {
@@ -187,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::mbar_arrive_expect_tx(&sm.q_full[st], 2 * kQHalf);
                     for (int hf = 0; hf < 2; ++hf)
-                        ptx::tma_load_4d(sm.q[st][hf], &tmq, hf * 64, t.g * kG, t.i0, t.b,
+                        ptx::tma_load_3d(sm.q[st][hf], &tmq, hf * 64, t.g * kG, t.start + i0,
                                          &sm.q_full[st]);
                     last_q = k;
                 }
@@ -200,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(&full[slot], 2 * kBlkHalf);
                     const int kp = key0 + kSwaBlockKeys * (s - cur.base);
                     for (int hf = 0; hf < 2; ++hf)
-                        ptx::tma_load_4d(ring + hf * kRingHalf + slot * kBlkHalf, map, hf * 64, t.g,
-                                         kp, t.b, &full[slot]);
+                        ptx::tma_load_3d(ring + hf * kRingHalf + slot * kBlkHalf, map, hf * 64, t.g,
+                                         t.start + kp, &full[slot]);
                     last_s = s;
                 }
             }
@@ -218,9 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA
         if (lane == 0 && !skip) {
             Issue is, ip;  // next S, next PV
+            is.t = ip.t = first;
             if (n > 0) {
-                is.advance(u0, n, nblk);
-                ip.advance(u0, n, nblk);
+                is.advance(n, Hkv);
+                ip.advance(n, Hkv);
             }
             const uint32_t kbase[2] = {ptx::smem_u32(sm.k[0]), ptx::smem_u32(sm.k[1])};
             const uint32_t vbase = ptx::smem_u32(sm.v[0]);
@@ -247,8 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::tc_commit(&sm.v_empty[b % kRing]);
                         issued = true;
                         prog = true;
-                        ++ip.k;
-                        if (ip.k < n) ip.advance(u0, n, nblk);
+                        if (++ip.k < n) {
+                            swa_cursor_next(ip.t, cu, B, T, total, Hkv);
+                            ip.advance(n, Hkv);
+                        }
                     }
                 }
                 // S = Q K^T for tile is.k: needs Q, its K blocks and a free slot
@@ -280,8 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ptx::tc_commit(&sm.k_empty[b % kRing]);
                         issued = true;
                         prog = true;
-                        ++is.k;
-                        if (is.k < n) is.advance(u0, n, nblk);
+                        if (++is.k < n) {
+                            swa_cursor_next(is.t, cu, B, T, total, Hkv);
+                            is.advance(n, Hkv);
+                        }
                     }
                 }
                 if (prog) {
@@ -309,11 +382,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + 256 * s + lane_off, tO = tS + kOCol;
         const int t_in = row / kG, hh = row % kG;
         const float sl2 = scale * kLog2e;
+        SwaTileCursor t = first;
+        if (s == 1 && n > 1) swa_cursor_next(t, cu, B, T, total, Hkv);
         for (int k = s; k < n; k += 2) {
+            if (k > s) {  // two tiles on: this slot takes every other tile
+                swa_cursor_next(t, cu, B, T, total, Hkv);
+                swa_cursor_next(t, cu, B, T, total, Hkv);
+            }
             const int ph = (k >> 1) & 1;
-            const Tile t = tile_at(u0 + k, nblk, Hkv);
-            const int key0 = t.i0 + kTT - kN;
-            const int qpos = t.i0 + t_in, h = t.g * kG + hh;
+            const int i0 = t.blk * kTT;
+            const int key0 = i0 + kTT - kN;
+            const int qpos = i0 + t_in, h = t.g * kG + hh;
             int c_lo, c_hi;
             swa_row_cols(qpos, key0, window, &c_lo, &c_hi);
             const bool interior = key0 >= 0;  // uniform over the tile
@@ -375,11 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_load_row<128>(tO, o);
             ptx::tc_fence_before();
             ptx::mbar_arrive(&sm.tmem_free[s]);  // the slot may take the next S now
-            const float inv = sink_all ? 0.f : 1.f / l;
-            if (qpos < T) {
+            const float inv = sink_all ? 0.f : vscale / l;  // the value scale rides on 1/l
+            if (qpos < t.len) {
                 const uint64_t inv2 = f2(inv, inv);
                 uint4 *dst = reinterpret_cast<uint4 *>(
-                    out + ((static_cast<long>(t.b) * T + qpos) * Hq + h) * 128);
+                    out + (static_cast<long>(t.start + qpos) * Hq + h) * 128);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     uint32_t w[4];
@@ -392,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 if (lse)
-                    lse[(static_cast<long>(t.b) * Hq + h) * T + qpos] =
+                    lse[lse_index(cu, t.b, h, qpos, t.start, T, total, Hq)] =
                         sink_all ? INFINITY : (mb + log2f(l)) * kLn2;
             }
         }
@@ -424,23 +503,26 @@ int prefill_swa_tc_supported(int G, int window) {
     return G == swa::kG && swa_pack_keys(G, window) == swa::kN;
 }
 
-int prefill_swa_grid(int B, int T, int Hkv) {
-    const long ntiles = static_cast<long>((T + swa::kTT - 1) / swa::kTT) * Hkv * B;
-    return static_cast<int>(ntiles < sm_count() ? ntiles : sm_count());
+int prefill_swa_grid(long max_tiles) {
+    return static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
 }
 
-cudaError_t launch_prefill_swa_tc(const PrefillMaps &maps, const float *sink, float *lse, int B,
-                                  int T, int Hq, int Hkv, int window, float scale,
-                                  unsigned int *err, cudaStream_t s) {
-    if (B == 0 || T == 0) return cudaSuccess;
+cudaError_t launch_prefill_swa_tc(const PrefillMaps &maps, const float *sink, float *lse,
+                                  const PrefillBatch &pb, int Hq, int Hkv, int window, float scale,
+                                  float vscale, unsigned int *err, cudaStream_t s) {
+    if (pb.B == 0 || pb.total == 0) return cudaSuccess;
+    // tiles: exact for equal lengths, an upper bound for a packed batch
+    const long max_tiles =
+        static_cast<long>(Hkv) * (pb.cu ? pb.total / swa::kTT + pb.B
+                                        : static_cast<long>(pb.B) * swa_seq_blocks(pb.T));
     const size_t smem = sizeof(swa::Smem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(swa::prefill_swa_stream_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    swa::prefill_swa_stream_kernel<<<prefill_swa_grid(B, T, Hkv), swa::kThreads, smem, s>>>(
-        maps.q, maps.k, maps.v, static_cast<__nv_bfloat16 *>(maps.out), sink, lse, B, T, Hq, Hkv,
-        window, scale, err);
+    swa::prefill_swa_stream_kernel<<<prefill_swa_grid(max_tiles), swa::kThreads, smem, s>>>(
+        maps.q, maps.k, maps.v, static_cast<__nv_bfloat16 *>(maps.out), sink, lse, pb.cu, pb.B,
+        pb.T, pb.total, Hq, Hkv, window, scale, vscale, err);
     return cudaGetLastError();
 }
 

@@ -85,15 +85,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_ga_kernel(const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv,
-                      const __grid_constant__ CUtensorMap tmo, const float *__restrict__ sink,
-                      float *__restrict__ lse, int B, int T, int Hq, int Hkv, int window,
-                      float scale, unsigned *err) {
+                      const __grid_constant__ CUtensorMap tmo, __nv_bfloat16 *__restrict__ out,
+                      const float *__restrict__ sink, float *__restrict__ lse,
+                      const int32_t *__restrict__ cu, int B, int T, int total, int Hq, int Hkv,
+                      int window, float scale, float vscale, unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // block -> (pair, head, batch); heaviest (latest) pairs first for causal balance
+    // block -> (pair, head, sequence); heaviest (latest) pairs first for causal
+    // balance.  T bounds every sequence: pairs past a sequence's end exit.
     const int npairs = (T + 255) / 256;
     const int per = Hq * B;
     const int pair = npairs - 1 - static_cast<int>(blockIdx.x) / per;
@@ -101,11 +103,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = (static_cast<int>(blockIdx.x) / Hq) % B;
     const int g = h / (Hq / Hkv);
     const int q0 = pair * 256;
+    const SeqSpan span = seq_span(cu, b, T, total);
+    if (q0 >= span.len) {  // uniform over the block: nothing to do
+        if (!span.ok && pair == npairs - 1 && h == 0 && threadIdx.x == 0) atomicOr(err, kErrSeqlens);
+        return;
+    }
+    const int len = span.len, start = span.start;
     int first[2], last[2];
     bool live[2];
     for (int t = 0; t < 2; ++t) {
-        live[t] = q0 + 128 * t < T;
-        ga_key_tiles(q0 + 128 * t, T, window, &first[t], &last[t]);
+        live[t] = q0 + 128 * t < len;
+        ga_key_tiles(q0 + 128 * t, len, window, &first[t], &last[t]);
     }
     if (!live[1]) { first[1] = first[0]; last[1] = first[0] - 1; }  // empty range
     const int jf = first[0];
@@ -146,17 +154,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(&sm.q_full, 2 * ntl * kTile);
             for (int t = 0; t < ntl; ++t)
                 for (int hf = 0; hf < 2; ++hf)
-                    ptx::tma_load_4d(sm.q[t][hf], &tmq, hf * 64, h, q0 + 128 * t, b, &sm.q_full);
+                    ptx::tma_load_3d(sm.q[t][hf], &tmq, hf * 64, h, start + q0 + 128 * t, &sm.q_full);
             for (int j = jf; ok && j <= jl; ++j) {
                 const int n = j - jf, st = n & 1;
                 if (n >= 2 && !ptx::mbar_wait(&sm.k_empty[st], ((n >> 1) - 1) & 1)) { ok = false; break; }
                 ptx::mbar_arrive_expect_tx(&sm.k_full[st], 2 * kTile);
                 for (int hf = 0; hf < 2; ++hf)
-                    ptx::tma_load_4d(sm.k[st][hf], &tmk, hf * 64, g, j * 128, b, &sm.k_full[st]);
+                    ptx::tma_load_3d(sm.k[st][hf], &tmk, hf * 64, g, start + j * 128, &sm.k_full[st]);
                 if (n >= 2 && !ptx::mbar_wait(&sm.v_empty[st], ((n >> 1) - 1) & 1)) { ok = false; break; }
                 ptx::mbar_arrive_expect_tx(&sm.v_full[st], 2 * kTile);
                 for (int hf = 0; hf < 2; ++hf)
-                    ptx::tma_load_4d(sm.v[st][hf], &tmv, hf * 64, g, j * 128, b, &sm.v_full[st]);
+                    ptx::tma_load_3d(sm.v[st][hf], &tmv, hf * 64, g, start + j * 128, &sm.v_full[st]);
             }
             if (!ok) atomicOr(err, kErrWait);
         }
@@ -286,20 +294,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ok && ptx::mbar_wait_warp(&sm.o_full[t], nlast & 1);
         if (ok) {
             ptx::tc_fence_after();
-            const float inv = (l > 0.f) ? 1.f / l : 0.f;
+            const float inv = (l > 0.f) ? vscale / l : 0.f;  // the value scale rides on 1/l
             store_o_row_smem(tO, inv, sm.q[t][0], sm.q[t][1], row);
             ptx::fence_proxy_async_smem();
         } else if (lane == 0) {
             atomicOr(err, kErrWait);
         }
         const bool wg_fail = ptx::named_bar_or(1 + t, 128, !ok);
-        if (row == 0 && !wg_fail) {
-            for (int hf = 0; hf < 2; ++hf) ptx::tma_store_4d(&tmo, sm.q[t][hf], hf * 64, h, qs, b);
-            ptx::bulk_commit();
-            ptx::bulk_wait_read0();
+        if (qs + 128 <= len) {  // a whole tile: one TMA store per D half
+            if (row == 0 && !wg_fail) {
+                for (int hf = 0; hf < 2; ++hf)
+                    ptx::tma_store_3d(&tmo, sm.q[t][hf], hf * 64, h, start + qs);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read0();
+            }
+        } else if (ok && qpos < len) {  // the sequence ends inside the tile: own row only
+            uint4 *dst = reinterpret_cast<uint4 *>(out + (static_cast<long>(start + qpos) * Hq + h) * 128);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                for (int lc = 0; lc < 8; ++lc)
+                    dst[hf * 8 + lc] = *reinterpret_cast<const uint4 *>(
+                        sm.q[t][hf] + row * kHalfRowBytes + ((lc ^ (row & 7)) << 4));
         }
-        if (ok && lse && qpos < T)
-            lse[(static_cast<long>(b) * Hq + h) * T + qpos] =
+        if (ok && lse && qpos < len)
+            lse[lse_index(cu, b, h, qpos, start, T, total, Hq)] =
                 (m == INFINITY) ? INFINITY : (m + log2f(l)) * kLn2;
     }
     ptx::tc_fence_before();
@@ -314,18 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill_ga_tc(const PrefillMaps &maps, const float *sink, float *lse, int B,
-                                 int T, int Hq, int Hkv, int window, float scale,
-                                 unsigned int *err, cudaStream_t s) {
-    if (B == 0 || T == 0) return cudaSuccess;
+cudaError_t launch_prefill_ga_tc(const PrefillMaps &maps, const float *sink, float *lse,
+                                 const PrefillBatch &pb, int Hq, int Hkv, int window, float scale,
+                                 float vscale, unsigned int *err, cudaStream_t s) {
+    if (pb.B == 0 || pb.T == 0 || pb.total == 0) return cudaSuccess;
     const size_t smem = sizeof(ga::Smem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(ga::prefill_ga_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const long blocks = static_cast<long>((T + 255) / 256) * Hq * B;
+    const long blocks = static_cast<long>((pb.T + 255) / 256) * Hq * pb.B;
     ga::prefill_ga_kernel<<<static_cast<unsigned>(blocks), ga::kThreads, smem, s>>>(
-        maps.q, maps.k, maps.v, maps.o, sink, lse, B, T, Hq, Hkv, window, scale, err);
+        maps.q, maps.k, maps.v, maps.o, static_cast<__nv_bfloat16 *>(maps.out), sink, lse, pb.cu,
+        pb.B, pb.T, pb.total, Hq, Hkv, window, scale, vscale, err);
     return cudaGetLastError();
 }
 

@@ -11,6 +11,7 @@ namespace tc {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kErrWait = 0x8u;
+constexpr unsigned kErrSeqlens = 0x10u;  // a packed batch gave an invalid sequence span
 constexpr int kHalfRowBytes = 128;  // one D half (64 bf16) per shared-memory row
 
 // Ties a register array to the preceding tcgen05.wait so that no use of the

@@ -22,6 +22,13 @@
  *   [MTP]    same announcement, figure "Multi-Token Prediction": the main model
  *            verifies token i and drafts i+1..i+3 in one pass and keeps the
  *            accepted prefix; summary section "MTP加速" (16K in / 1K out).
+ *   [SERVE]  summary section "MTP加速": serving measured with 16K-token prompts
+ *            at several in-node batch sizes (batches of prompts of unequal
+ *            length, packed here by cu_seqlens).
+ *   [CFG]    dpshk.com article on MiMo-V2-Flash-Base ("小米AI团队揭秘"), section
+ *            "轻量级多token预测技术": config.json lists attention_value_scale =
+ *            0.707 without saying what it scales; read here as a factor on the
+ *            attention output (equivalently on V).
  *
  * Definition (all entry points):  for query position i of head h (kv head
  * g = h / (Hq/Hkv)), visible keys j satisfy 0 <= j <= i and, for SWA,
@@ -74,6 +81,7 @@ typedef enum attn_dtype {
 #define ATTN_DEVERR_CTX_OOB      0x2u  /* seq_len > max_ctx, > max_pages*page_size, or < q_len */
 #define ATTN_DEVERR_QLEN         0x4u  /* cu_q gives q_len > q_max                          */
 #define ATTN_DEVERR_WAIT_TIMEOUT 0x8u  /* an in-kernel pipeline wait exceeded its time limit  */
+#define ATTN_DEVERR_SEQLENS      0x10u /* a packed prefill batch gave an invalid sequence span */
 
 /* Library version (major*10000 + minor*100 + patch). */
 int attn_version(void);
@@ -105,6 +113,30 @@ attn_status_t attn_swa_sink_prefill(const void *q, const void *k, const void *v,
 attn_status_t attn_ga_sink_prefill(const void *q, const void *k, const void *v, const float *sink,
                                    void *o, float *lse, int B, int T, int Hq, int Hkv, int D,
                                    float scale, attn_dtype_t dtype, void *stream);
+
+/* Packed (variable-length) prefill [ARCH][SINK][SERVE], with the output scale
+ * of the model configuration [CFG] (attention_value_scale).
+ *   q [total,Hq,D], k [total,Hkv,D], v [total,Hkv,D], o [total,Hq,D]   (dtype)
+ *   cu_seqlens [B+1] int32 on the device: sequence b is tokens cu_seqlens[b] ..
+ *     cu_seqlens[b+1]-1 with positions 0 .. len-1; cu_seqlens[0] = 0 and
+ *     cu_seqlens[B] = total_tokens.  Sequences never see each other's keys.
+ *   max_seqlen >= every length (sizes the grid);  lse [Hq,total] fp32 or NULL
+ *   value_scale multiplies the output (o = value_scale * sum_j p_ij v_j; the
+ *     LSE is unscaled); 1 gives the plain definition.
+ * A span that is decreasing, outside [0, total_tokens) or longer than
+ * max_seqlen is skipped (its rows are not written) and sets
+ * ATTN_DEVERR_SEQLENS.  Everything else as in the calls above (same dtype,
+ * D and kernel support; the sliding-window form keeps window >= 1). */
+attn_status_t attn_swa_sink_prefill_varlen(const void *q, const void *k, const void *v,
+                                           const int32_t *cu_seqlens, const float *sink, void *o,
+                                           float *lse, int B, int total_tokens, int max_seqlen,
+                                           int Hq, int Hkv, int D, int window, float scale,
+                                           float value_scale, attn_dtype_t dtype, void *stream);
+attn_status_t attn_ga_sink_prefill_varlen(const void *q, const void *k, const void *v,
+                                          const int32_t *cu_seqlens, const float *sink, void *o,
+                                          float *lse, int B, int total_tokens, int max_seqlen,
+                                          int Hq, int Hkv, int D, float scale, float value_scale,
+                                          attn_dtype_t dtype, void *stream);
 
 /* ------------------------------------------------------------ KV caches ---
  * SWA ring [KV][MTP]: ring_k, ring_v [B,Hkv,R,D] with R = ring_slots >=

@@ -8,7 +8,8 @@ does.  It shares no code with the CUDA library in
 Contents
 --------
 - ``prefill`` / ``prefill_rows`` / ``verify``: ctypes wrappers over the plain C
-  implementation in ``attn_sink_oracle.c`` (fp64 loops, OpenMP over rows).
+  implementation in ``attn_sink_oracle.c`` (fp64 loops, OpenMP over rows);
+  ``prefill_varlen`` applies ``prefill`` to each sequence of a packed batch.
 - ``brute``: a second formulation in numpy (full score matrix, an appended sink
   column, a library softmax) used to pin the C code on tiny inputs.
 - ``index``: the integer definitions the kernels' index arithmetic must
@@ -138,6 +139,35 @@ def prefill_rows(q, k, v, sink, rows, window: int | None, scale: float | None = 
                                      B, T, Hq, Hkv, D, int(window or 0), scale)
     if rc != 0:
         raise ValueError("oracle_prefill_rows rejected its arguments")
+    return (o, lse) if want_lse else o
+
+
+def prefill_varlen(q, k, v, cu_seqlens, sink, window: int | None, scale: float | None = None,
+                   value_scale: float = 1.0, want_lse: bool = False):
+    """Prefill of a packed batch: q [total,Hq,D], k/v [total,Hkv,D], sequence b
+    = tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 with positions 0..len-1, each
+    sequence attending only to itself (the plain definition per sequence).
+    The output is multiplied by value_scale: the reading of the model
+    configuration's attention_value_scale (dpshk.com article on
+    MiMo-V2-Flash-Base, section "轻量级多token预测技术") as a factor on the
+    attention output; the LSE is unscaled.
+    Returns o (fp64 [total,Hq,D]) and, on request, lse (fp64 [Hq,total])."""
+    q, k, v, sink = _f32(q), _f32(k), _f32(v), _f32(sink)
+    cu = _i32(cu_seqlens)
+    total, Hq, D = q.shape
+    if (cu.ndim != 1 or cu.shape[0] < 1 or cu[0] != 0 or cu[-1] != total
+            or np.any(np.diff(cu) < 0) or k.shape[0] != total or v.shape != k.shape):
+        raise ValueError("oracle.prefill_varlen: inconsistent shapes or offsets")
+    o = np.zeros((total, Hq, D), np.float64)
+    lse = np.zeros((Hq, total), np.float64)
+    for b in range(cu.shape[0] - 1):
+        s, e = int(cu[b]), int(cu[b + 1])
+        if e == s:
+            continue
+        ob, lb = prefill(q[None, s:e], k[None, s:e], v[None, s:e], sink, window, scale,
+                         want_lse=True)
+        o[s:e] = float(value_scale) * ob[0]
+        lse[:, s:e] = lb[0]
     return (o, lse) if want_lse else o
 
 

@@ -39,6 +39,29 @@ def prefill_inputs(B: int, T: int, Hq: int, Hkv: int, D: int, seed: int,
     return q, k, v, sink
 
 
+def packed_lengths(n: int, lo: int, hi: int, seed: int) -> np.ndarray:
+    """n sequence lengths, log-uniform in [lo, hi] (a serving batch of prompts
+    of mixed length), int32."""
+    rng = np.random.Generator(np.random.Philox(int(seed)))
+    x = np.exp(rng.uniform(np.log(lo), np.log(hi + 1), size=n))
+    return np.clip(np.floor(x), lo, hi).astype(np.int32)
+
+
+def packed_inputs(lens, Hq: int, Hkv: int, D: int, seed: int, dtype=torch.bfloat16,
+                  device="cpu"):
+    """A packed batch: q [total,Hq,D], k/v [total,Hkv,D] in `dtype`, sink [Hq]
+    fp32 and cu_seqlens [B+1] int32 (numpy) with cu[0] = 0."""
+    lens = np.asarray(lens, np.int64)
+    total = int(lens.sum())
+    g = _gen(seed, device)
+    q = torch.randn(total, Hq, D, generator=g, device=device).to(dtype)
+    k = torch.randn(total, Hkv, D, generator=g, device=device).to(dtype)
+    v = torch.randn(total, Hkv, D, generator=g, device=device).to(dtype)
+    sink = torch.randn(Hq, generator=g, device=device)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    return q, k, v, sink, cu
+
+
 def sink_logits(Hq: int, seed: int, device="cpu") -> torch.Tensor:
     return torch.randn(Hq, generator=_gen(seed, device), device=device)
 

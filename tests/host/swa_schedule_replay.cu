@@ -1,34 +1,38 @@
 // Host-side replay of the streaming SWA prefill schedule, built from the same
 // index functions the kernel runs (index_math.cuh compiled as host code), so
 // that the CPU test suite checks the run partition, the ring bookkeeping and
-// the column masks without a GPU.  visits [B*Hkv, T, T+1]; column T counts
-// admitted keys outside [0, T).  Returns the largest number of blocks that are
+// the column masks without a GPU, for batches of equal length (cu = NULL) and
+// packed batches (cu[B+1], T >= the longest sequence).  visits [B*Hkv, T, T+1]
+// by position within the sequence; column T counts admitted keys outside the
+// sequence.  Returns the largest number of blocks that are
 // live (loaded and not yet released) at any point of a run.
 #include "index_math.cuh"
 
-extern "C" int swa_stream_visits_host(int32_t *visits, int B, int T, int Hkv, int window,
-                                      int grid) {
+extern "C" int swa_stream_visits_host(int32_t *visits, const int32_t *cu, int B, int T,
+                                      int total, int Hkv, int window, int grid) {
     using namespace attn;
-    const int nblk = (T + kSwaTokens - 1) / kSwaTokens;
-    const int ntiles = nblk * Hkv * B;
+    const int ntiles = swa_total_tiles(cu, B, T, total, Hkv);
     int max_live = 0;
     for (int cta = 0; cta < grid; ++cta) {
         int u0, u1;
         swa_stream_range(cta, grid, ntiles, &u0, &u1);
+        if (u0 >= u1) continue;
         SwaRingCursor cur;
+        SwaTileCursor t = swa_cursor_at(cu, B, T, total, Hkv, u0);
         int slot_key[kSwaRingBlocks];
         for (int s = 0; s < kSwaRingBlocks; ++s) slot_key[s] = -(1 << 30);
         int released = 0;  // blocks [0, released) were released
         for (int u = u0; u < u1; ++u) {
-            const int bg = u / nblk, i0 = (u - bg * nblk) * kSwaTokens;
+            if (u > u0) swa_cursor_next(t, cu, B, T, total, Hkv);
+            const int bg = t.b * Hkv + t.g, i0 = t.blk * kSwaTokens;
             const int key0 = i0 + kSwaTokens - kSwaKeys;
             swa_ring_step(cur, bg, kSwaTileBlocks);
             for (int s = cur.first_new; s < cur.first_new + cur.n_new; ++s)
                 slot_key[s % kSwaRingBlocks] = key0 + kSwaBlockKeys * (s - cur.base);
             if (cur.seq_next - released > max_live) max_live = cur.seq_next - released;
             const bool interior = key0 >= 0;
-            for (int t = 0; t < kSwaTokens && i0 + t < T; ++t) {
-                const int qpos = i0 + t;
+            for (int tt = 0; tt < kSwaTokens && i0 + tt < t.len; ++tt) {
+                const int qpos = i0 + tt;
                 int c_lo, c_hi;
                 swa_row_cols(qpos, key0, window, &c_lo, &c_hi);
                 int32_t *row = visits + (static_cast<long>(bg) * T + qpos) * (T + 1);
@@ -37,11 +41,11 @@ extern "C" int swa_stream_visits_host(int32_t *visits, int B, int T, int Hkv, in
                     for (int cc = 0; cc < kSwaBlockKeys; ++cc) {
                         if (!swa_col_admitted(j * kSwaBlockKeys + cc, c_lo, c_hi, interior)) continue;
                         const int key = kb + cc;
-                        row[(key >= 0 && key < T) ? key : T] += 1;
+                        row[(key >= 0 && key < t.len) ? key : T] += 1;
                     }
                 }
             }
-            const bool next_same = (u + 1 < u1) && ((u + 1) / nblk == bg);
+            const bool next_same = (u + 1 < u1) && (t.blk + 1 < t.nblk);
             released = swa_ring_release_end(cur.base, next_same, kSwaTileBlocks);
         }
     }

@@ -2,7 +2,8 @@
 functions (index_math.cuh compiled as host code):
 - the streaming SWA prefill schedule must admit every visible (query, key)
   pair exactly once across the CTA runs and the shared-memory ring of 16-key
-  blocks, and never need more live blocks than the ring holds;
+  blocks, and never need more live blocks than the ring holds, for batches of
+  equal length and for packed batches (cu_seqlens);
 - the ring verify's visible slots (two slot intervals) must be exactly the
   slots holding positions in the query's window.
 No GPU needed; the same functions run on the device in test_gpu_index."""
@@ -30,14 +31,21 @@ def replay():
                         SRC, "-o", LIB], check=True)
     lib = ctypes.CDLL(LIB)
     f = lib.swa_stream_visits_host
-    f.argtypes = [np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")] + [ctypes.c_int] * 5
+    f.argtypes = [np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS"), ctypes.c_void_p] + \
+        [ctypes.c_int] * 6
     f.restype = ctypes.c_int
     lib.ring_visible_host.argtypes = [np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")] + [ctypes.c_int] * 4
     lib.ring_visible_host.restype = None
 
-    def run(B, T, Hkv, window, grid):
+    def run(B, T, Hkv, window, grid, cu=None):
+        """cu: packed batch offsets [B+1] (T = the longest sequence), or None."""
         visits = np.zeros((B * Hkv, T, T + 1), np.int32)
-        live = f(visits, B, T, Hkv, window, grid)
+        if cu is None:
+            live = f(visits, None, B, T, B * T, Hkv, window, grid)
+        else:
+            cu = np.ascontiguousarray(cu, np.int32)
+            live = f(visits, cu.ctypes.data_as(ctypes.c_void_p), B, T, int(cu[-1]), Hkv, window,
+                     grid)
         return visits, live
     run.ring_visible = lib.ring_visible_host
     return run
@@ -63,6 +71,36 @@ def test_schedule_admits_each_visible_pair_once(replay, B, T, Hkv, window, grid)
         np.testing.assert_array_equal(visits[bg, :, :T], exp, err_msg=f"bg={bg}")
         assert not visits[bg, :, T].any()
     assert live <= RING_BLOCKS
+
+
+@pytest.mark.parametrize("lens,Hkv,window,grid", [
+    ([5, 0, 40, 16, 17], 2, 128, 3), ([300, 1, 0, 0, 129], 1, 128, 148),
+    ([0, 0, 7], 3, 120, 2), ([1000, 200, 33], 2, 114, 7), ([2], 1, 129, 1),
+])
+def test_packed_schedule_admits_each_visible_pair_once(replay, lens, Hkv, window, grid):
+    """Packed batches: each sequence starts its own tile grid; keys outside the
+    sequence (before its first token or past its end) are never admitted, and
+    empty sequences take no tiles."""
+    B, T = len(lens), max(max(lens), 1)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ntiles = Hkv * sum((n + 15) // 16 for n in lens)
+    visits, live = replay(B, T, Hkv, window, max(1, min(grid, ntiles)), cu)
+    for b, n in enumerate(lens):
+        exp = _expected(n, window)
+        for g in range(Hkv):
+            v = visits[b * Hkv + g]
+            np.testing.assert_array_equal(v[:n, :n], exp, err_msg=f"b={b} g={g}")
+            assert not v[:n, n:].any() and not v[n:].any()
+    assert live <= RING_BLOCKS
+
+
+def test_packed_equal_lengths_match_the_unpacked_replay(replay):
+    lens = [123, 123, 123]
+    cu = np.array([0, 123, 246, 369], np.int32)
+    a, la = replay(3, 123, 2, 128, 5)
+    b, lb = replay(3, 123, 2, 128, 5, cu)
+    np.testing.assert_array_equal(a, b)
+    assert la == lb
 
 
 def test_replay_catches_a_wrong_window(replay):
