@@ -14,6 +14,9 @@ Contents
   column, a library softmax) used to pin the C code on tiny inputs.
 - ``index``: the integer definitions the kernels' index arithmetic must
   reproduce bit for bit (visibility, ring slot, page location).
+- ``fp8``: the E4M3 codes of an 8-bit KV cache (decode, encode with
+  round-to-nearest-even and saturation, per-kv-head scales); ``verify_fp8``
+  is ``verify`` over the dequantized history.
 
 Method sources: MiMo-V2-Flash technical-report summary (fanfer.top,
 "MiMo-V2"), sections "MiMo-V2-Flash Model Architecture" (W = 128, 5:1 hybrid)
@@ -31,7 +34,7 @@ import threading
 
 import numpy as np
 
-from . import brute, index  # noqa: F401  (re-exported)
+from . import brute, fp8, index  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_sink_oracle.c")
@@ -191,3 +194,19 @@ def verify(q, cu_q, k_hist, v_hist, seq_lens, sink, window: int | None,
         raise ValueError("oracle_verify rejected its arguments")
     out = [o] + ([lse] if want_lse else []) + ([ps] if want_psink else [])
     return out[0] if len(out) == 1 else tuple(out)
+
+
+def verify_fp8(q, cu_q, k_codes, v_codes, k_scale, v_scale, seq_lens, sink,
+               window: int | None = None, scale: float | None = None):
+    """MTP verify over an 8-bit (E4M3) history: k_codes/v_codes uint8
+    [B,Lmax,Hkv,D], k_scale/v_scale [Hkv]; the cache holds code * scale of
+    its kv head, so the result is ``verify`` on that dequantized history
+    (rounded to fp32, ~6e-8 relative, for the C oracle)."""
+    k_codes, v_codes = np.asarray(k_codes, np.uint8), np.asarray(v_codes, np.uint8)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    Hkv = k_codes.shape[2]
+    if ks.shape != (Hkv,) or vs.shape != (Hkv,) or v_codes.shape != k_codes.shape:
+        raise ValueError("oracle.verify_fp8: inconsistent shapes")
+    kd = (fp8.decode(k_codes) * ks.astype(np.float64)[None, None, :, None]).astype(np.float32)
+    vd = (fp8.decode(v_codes) * vs.astype(np.float64)[None, None, :, None]).astype(np.float32)
+    return verify(q, cu_q, kd, vd, seq_lens, sink, window, scale)
