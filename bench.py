@@ -371,7 +371,7 @@ def bench_prefill_e2e(A, synth, steps: int, warmup: int, world: int, stream, see
     return ms, h2d, d2h
 
 
-def _paged_problem(ctx, q_lens, seed, device="cuda"):
+def _paged_problem(ctx, q_lens, seed, device="cuda", fp8=False):
     import torch
     import synth
     npages = (ctx + PAGE - 1) // PAGE
@@ -383,25 +383,38 @@ def _paged_problem(ctx, q_lens, seed, device="cuda"):
     for b in range(nb):
         pt[b, :npages[b]] = perm[o:o + npages[b]]
         o += npages[b]
-    kp = synth.normal((num_pages, HKV, PAGE, D), seed + 1, device=device)
-    vp = synth.normal((num_pages, HKV, PAGE, D), seed + 2, device=device)
+    if fp8:   # E4M3 codes and per-kv-head scales
+        kp = synth.e4m3_codes((num_pages, HKV, PAGE, D), seed + 1, device=device)
+        vp = synth.e4m3_codes((num_pages, HKV, PAGE, D), seed + 2, device=device)
+    else:
+        kp = synth.normal((num_pages, HKV, PAGE, D), seed + 1, device=device)
+        vp = synth.normal((num_pages, HKV, PAGE, D), seed + 2, device=device)
     cu_q = synth.cu_seqlens(q_lens)
     q = synth.normal((int(cu_q[-1]), HQ, D), seed + 3, device=device)
     sink = synth.sink_logits(HQ, seed + 4, device=device)
     return dict(kp=kp, vp=vp, pt=torch.from_numpy(pt).to(device), ctx=torch.from_numpy(ctx).to(device),
-                cu_q=torch.from_numpy(cu_q).to(device), q=q, sink=sink, max_ctx=int(ctx.max()))
+                cu_q=torch.from_numpy(cu_q).to(device), q=q, sink=sink, max_ctx=int(ctx.max()),
+                ks=synth.kv_scales(HKV, seed + 5, device=device),
+                vs=synth.kv_scales(HKV, seed + 6, device=device))
 
 
-def bench_verify_ga(A, ctx, q_lens, steps, warmup, world, stream, seed):
+def bench_verify_ga(A, ctx, q_lens, steps, warmup, world, stream, seed, fp8=False):
+    """GA paged verify; fp8=True reads 8-bit (E4M3) pages: half the bytes."""
     import torch
-    P = _paged_problem(ctx, q_lens, seed)
+    P = _paged_problem(ctx, q_lens, seed, fp8=fp8)
     ws_bytes = A.attn_ga_sink_verify_workspace(len(ctx), HQ, HKV, D, QMAX, P["max_ctx"])
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(P["q"])
 
     def step(_):
-        A.attn_ga_sink_verify(P["q"], P["cu_q"], P["kp"], P["vp"], P["pt"], P["ctx"], P["sink"],
-                              max_ctx=P["max_ctx"], q_max=QMAX, out=out, workspace=ws, stream=stream)
+        if fp8:
+            A.attn_ga_sink_verify_fp8(P["q"], P["cu_q"], P["kp"], P["vp"], P["pt"], P["ctx"],
+                                      P["sink"], P["ks"], P["vs"], max_ctx=P["max_ctx"], q_max=QMAX,
+                                      out=out, workspace=ws, stream=stream)
+        else:
+            A.attn_ga_sink_verify(P["q"], P["cu_q"], P["kp"], P["vp"], P["pt"], P["ctx"], P["sink"],
+                                  max_ctx=P["max_ctx"], q_max=QMAX, out=out, workspace=ws,
+                                  stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -409,7 +422,7 @@ def bench_verify_ga(A, ctx, q_lens, steps, warmup, world, stream, seed):
         ms = time_region(step, steps, world, stream)
     if A.attn_check_device_error(stream) != 0:
         raise RuntimeError("GA verify reported a device error")
-    return ms, verify_kv_bytes(ctx)
+    return ms, verify_kv_bytes(ctx) / (2 if fp8 else 1)
 
 
 def bench_verify_swa(A, nreq, steps, warmup, world, stream, seed):
@@ -541,6 +554,14 @@ def main():
                                     "calls_per_s": 1e3 / ms4, "ms": ms4,
                                     "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
                                                  "frac": kv4 / (ms4 * 1e-3) / 1e9 / hbm}}
+        ms8, kv8 = bench_verify_ga(A, ctx4, np.full(64, QMAX, np.int32), args.steps, warmup, world,
+                                   stream, 1004 + 10 * rank, fp8=True)
+        parts["verify_ga_fp8_64req"] = {"config": "64 req x q4, ctx~U[4096,65536], page 64, E4M3 pages",
+                                        "value": kv8 / (ms8 * 1e-3) / 1e9, "unit": "GB/s",
+                                        "calls_per_s": 1e3 / ms8, "ms": ms8,
+                                        "speedup_vs_bf16_pages": ms4 / ms8,
+                                        "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                                                     "frac": kv8 / (ms8 * 1e-3) / 1e9 / hbm}}
         ms_s, kv_s = bench_verify_swa(A, 64, args.steps, warmup, world, stream, 2004 + 10 * rank)
         parts["verify_swa_64req_39layers"] = {
             "config": "64 req x q4, 131-slot ring, 39 layers in one CUDA graph",
@@ -603,13 +624,15 @@ def main():
 
 def run_profile(A, synth, args, warmup, stream):
     """Only the named kernels, for profiler captures (sizes: the headline and
-    GA prefill at full size, 1.2 GB each; GA verify on 16 requests ~ 2.3 GB)."""
+    GA prefill at full size, 1.2 GB each; GA verify on 16 requests ~ 2.3 GB,
+    half that with 8-bit pages)."""
     for name in args.profile.split(","):
         if name in ("swa", "ga"):
             bench_prefill(A, synth, name, args.steps, warmup, 1, stream, 1002)
-        elif name == "verify_ga":
+        elif name in ("verify_ga", "verify_ga_fp8"):
             ctx = synth.context_lengths(16, 4096, 65536, 1004)
-            bench_verify_ga(A, ctx, np.full(16, QMAX, np.int32), args.steps, warmup, 1, stream, 1004)
+            bench_verify_ga(A, ctx, np.full(16, QMAX, np.int32), args.steps, warmup, 1, stream, 1004,
+                            fp8=name.endswith("fp8"))
         elif name == "verify_swa":
             bench_verify_swa(A, 64, args.steps, warmup, 1, stream, 2004)
         else:

@@ -53,6 +53,8 @@ _SIGS = {
     "attn_swa_sink_verify": ([_vp] * 7 + [_ci] * 7 + [_cf, _ci, _vp], _ci),
     "attn_ga_sink_verify_workspace": ([_ci] * 6, _sz),
     "attn_ga_sink_verify": ([_vp] * 5 + [_ci] * 3 + [_vp] * 4 + [_sz] + [_ci] * 6 + [_cf, _ci, _vp], _ci),
+    "attn_ga_paged_append_fp8": ([_vp] * 7 + [_ci] * 3 + [_vp, _vp] + [_ci] * 4 + [_vp], _ci),
+    "attn_ga_sink_verify_fp8": ([_vp] * 5 + [_ci] * 3 + [_vp] * 6 + [_sz] + [_ci] * 6 + [_cf, _vp], _ci),
     "attn_ga_sink_verify_noalloc": ([_vp] * 5 + [_ci] * 3 + [_vp] * 3 + [_ci] * 6 + [_cf, _ci, _vp], _ci),
     "attn_debug_prefill_visits": ([_vp] + [_ci] * 4 + [_vp], _ci),
     "attn_debug_swa_stream_visits": ([_vp] + [_ci] * 5 + [_vp], _ci),
@@ -277,6 +279,53 @@ def attn_ga_sink_verify(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, m
                                     D, int(q_max), int(max_ctx), scale, _dtype_code(q),
                                     _stream(stream)))
     return out
+
+
+def attn_ga_sink_verify_fp8(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, k_scale,
+                            v_scale, max_ctx: int, q_max: int = 4, scale: float | None = None,
+                            out=None, workspace=None, stream=None):
+    """MTP verify against an 8-bit (E4M3) GA paged cache: k_pages/v_pages uint8
+    [P,Hkv,page,D] codes, entry = code * k_scale[g] (v_scale[g]); q/o bf16."""
+    _cuda(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, k_scale, v_scale, out, workspace)
+    if k_pages.dtype != torch.uint8 or v_pages.dtype != torch.uint8:
+        raise TypeError("8-bit pages are uint8 E4M3 codes")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
+        raise TypeError("k_scale/v_scale are float32 [Hkv]")
+    nq, Hq, D = q.shape
+    P, Hkv, page_size, _ = k_pages.shape
+    B, max_pages = page_table.shape
+    out = torch.empty_like(q) if out is None else out
+    need = attn_ga_sink_verify_workspace(B, Hq, Hkv, D, q_max, max_ctx)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(_lib.attn_ga_sink_verify_fp8(_ptr(q), _ptr(cu_q), _ptr(k_pages), _ptr(v_pages),
+                                        _ptr(page_table), max_pages, P, page_size, _ptr(seq_lens),
+                                        _ptr(sink), _ptr(k_scale), _ptr(v_scale), _ptr(out),
+                                        _ptr(workspace), ws_bytes, B, Hq, Hkv, D, int(q_max),
+                                        int(max_ctx), scale, _stream(stream)))
+    return out
+
+
+def attn_ga_paged_append_fp8(k_new, v_new, cu_q, seq_lens, k_pages, v_pages, page_table,
+                             k_scale, v_scale, q_max: int, stream=None):
+    """Quantize each request's new bf16 keys/values to E4M3 codes of
+    value / scale[kv head] and write them into its 8-bit pages."""
+    _cuda(k_new, v_new, cu_q, seq_lens, k_pages, v_pages, page_table, k_scale, v_scale)
+    if k_new.dtype != torch.bfloat16 or v_new.dtype != torch.bfloat16 or k_new.shape != v_new.shape:
+        raise TypeError("new keys/values are bf16 [rows,Hkv,D]")
+    if k_pages.dtype != torch.uint8 or v_pages.shape != k_pages.shape:
+        raise TypeError("8-bit pages are uint8 [P,Hkv,page,D]")
+    if cu_q.dtype != torch.int32 or seq_lens.dtype != torch.int32 or page_table.dtype != torch.int32:
+        raise TypeError("cu_q, seq_lens and page_table are int32")
+    B = seq_lens.shape[0]
+    Hkv, D = k_new.shape[1], k_new.shape[2]
+    _check(_lib.attn_ga_paged_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(seq_lens),
+                                         _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                         page_table.shape[1], k_pages.shape[0], k_pages.shape[2],
+                                         _ptr(k_scale), _ptr(v_scale), B, Hkv, D, int(q_max),
+                                         _stream(stream)))
 
 
 def attn_ga_sink_verify_noalloc(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink,

@@ -289,6 +289,27 @@ ATTN_EXPORT attn_status_t attn_ga_paged_append(const void *k_new, const void *v_
     return e == cudaSuccess ? ok() : cuda_fail(e, "paged append launch");
 }
 
+ATTN_EXPORT attn_status_t attn_ga_paged_append_fp8(
+    const void *k_new, const void *v_new, const int32_t *cu_q, const int32_t *seq_lens,
+    void *k_pages, void *v_pages, const int32_t *page_table, int max_pages, int num_pages,
+    int page_size, const float *k_scale, const float *v_scale, int B, int Hkv, int D, int q_max,
+    void *stream) {
+    attn_status_t st = check_append(k_new, v_new, cu_q, seq_lens, k_pages, v_pages, B, Hkv, D,
+                                    q_max, ATTN_BF16);
+    if (st != ATTN_OK) return st;
+    if (!k_scale || !v_scale) return fail(ATTN_ERR_INVALID_ARG, "null pointer argument");
+    if (D != 128) return fail(ATTN_ERR_UNSUPPORTED, "the 8-bit cache needs D = 128 (got %d)", D);
+    if (!page_table || max_pages < 1 || num_pages < 1 || page_size < 1)
+        return fail(ATTN_ERR_INVALID_ARG, "bad page table arguments");
+    unsigned *err = device_error_word();
+    if (!err) return fail(ATTN_ERR_CUDA, "no CUDA device / error word unavailable");
+    cudaError_t e = attn::launch_paged_append_fp8(k_new, v_new, cu_q, seq_lens, k_pages, v_pages,
+                                                  page_table, max_pages, num_pages, page_size,
+                                                  k_scale, v_scale, B, Hkv, q_max, err,
+                                                  as_stream(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "fp8 paged append launch");
+}
+
 ATTN_EXPORT attn_status_t attn_swa_sink_verify(const void *q, const int32_t *cu_q,
                                                const void *ring_k, const void *ring_v,
                                                const int32_t *seq_lens, const float *sink, void *o,
@@ -343,14 +364,16 @@ ATTN_EXPORT size_t attn_ga_sink_verify_workspace(int B, int Hq, int Hkv, int D, 
            ws_segment(units * attn::kVerifyRows * 2 * sizeof(float));
 }
 
-ATTN_EXPORT attn_status_t attn_ga_sink_verify(const void *q, const int32_t *cu_q,
-                                              const void *k_pages, const void *v_pages,
-                                              const int32_t *page_table, int max_pages,
-                                              int num_pages, int page_size,
-                                              const int32_t *seq_lens, const float *sink, void *o,
-                                              void *workspace, size_t workspace_bytes, int B,
-                                              int Hq, int Hkv, int D, int q_max, int max_ctx,
-                                              float scale, attn_dtype_t dtype, void *stream) {
+namespace {
+// GA paged verify, bf16 pages (k_scale == nullptr) or E4M3 pages with
+// per-kv-head scales.
+attn_status_t ga_verify_common(const void *q, const int32_t *cu_q, const void *k_pages,
+                               const void *v_pages, const int32_t *page_table, int max_pages,
+                               int num_pages, int page_size, const int32_t *seq_lens,
+                               const float *sink, void *o, void *workspace,
+                               size_t workspace_bytes, int B, int Hq, int Hkv, int D, int q_max,
+                               int max_ctx, float scale, attn_dtype_t dtype, const float *k_scale,
+                               const float *v_scale, void *stream) {
     attn_status_t st = check_verify(q, cu_q, seq_lens, sink, o, k_pages, v_pages, B, Hq, Hkv, D,
                                     q_max, scale, dtype);
     if (st != ATTN_OK) return st;
@@ -368,13 +391,17 @@ ATTN_EXPORT attn_status_t attn_ga_sink_verify(const void *q, const int32_t *cu_q
     unsigned *err = device_error_word();
     if (!err) return fail(ATTN_ERR_CUDA, "no CUDA device / error word unavailable");
     attn::VerifyMaps maps;
+    const bool fp8 = k_scale != nullptr;
+    const uint64_t row = fp8 ? 128 : 256;  // bytes per cached token of one kv head
     uint64_t dims[4] = {128, static_cast<uint64_t>(page_size), static_cast<uint64_t>(Hkv),
                         static_cast<uint64_t>(num_pages)};
-    uint64_t strides[3] = {256, static_cast<uint64_t>(page_size) * 256,
-                           static_cast<uint64_t>(Hkv) * page_size * 256};
-    uint32_t box[4] = {64, static_cast<uint32_t>(attn::kVerifyBlock), 1, 1};
-    if (!make_map_4d(&maps.k, k_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, strides, box) ||
-        !make_map_4d(&maps.v, v_pages, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dims, strides, box))
+    uint64_t strides[3] = {row, static_cast<uint64_t>(page_size) * row,
+                           static_cast<uint64_t>(Hkv) * page_size * row};
+    uint32_t box[4] = {fp8 ? 128u : 64u, static_cast<uint32_t>(attn::kVerifyBlock), 1, 1};
+    const CUtensorMapDataType dt =
+        fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_map_4d(&maps.k, k_pages, dt, dims, strides, box) ||
+        !make_map_4d(&maps.v, v_pages, dt, dims, strides, box))
         return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the page maps");
     const int nsplit =
         attn::verify_num_splits(max_ctx, attn::kVerifyChunkPages * attn::kVerifyBlock);
@@ -387,8 +414,35 @@ ATTN_EXPORT attn_status_t attn_ga_sink_verify(const void *q, const int32_t *cu_q
     }
     cudaError_t e = attn::launch_verify_paged(maps, q, cu_q, seq_lens, page_table, max_pages,
                                               num_pages, sink, o, ws_o, ws_ml, nsplit, B, Hq, Hkv,
-                                              q_max, max_ctx, scale, err, as_stream(stream));
+                                              q_max, max_ctx, scale, k_scale, v_scale, err,
+                                              as_stream(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "ga verify launch");
+}
+}  // namespace
+
+ATTN_EXPORT attn_status_t attn_ga_sink_verify(const void *q, const int32_t *cu_q,
+                                              const void *k_pages, const void *v_pages,
+                                              const int32_t *page_table, int max_pages,
+                                              int num_pages, int page_size,
+                                              const int32_t *seq_lens, const float *sink, void *o,
+                                              void *workspace, size_t workspace_bytes, int B,
+                                              int Hq, int Hkv, int D, int q_max, int max_ctx,
+                                              float scale, attn_dtype_t dtype, void *stream) {
+    return ga_verify_common(q, cu_q, k_pages, v_pages, page_table, max_pages, num_pages,
+                            page_size, seq_lens, sink, o, workspace, workspace_bytes, B, Hq, Hkv,
+                            D, q_max, max_ctx, scale, dtype, nullptr, nullptr, stream);
+}
+
+ATTN_EXPORT attn_status_t attn_ga_sink_verify_fp8(
+    const void *q, const int32_t *cu_q, const void *k_pages, const void *v_pages,
+    const int32_t *page_table, int max_pages, int num_pages, int page_size,
+    const int32_t *seq_lens, const float *sink, const float *k_scale, const float *v_scale,
+    void *o, void *workspace, size_t workspace_bytes, int B, int Hq, int Hkv, int D, int q_max,
+    int max_ctx, float scale, void *stream) {
+    if (!k_scale || !v_scale) return fail(ATTN_ERR_INVALID_ARG, "null pointer argument");
+    return ga_verify_common(q, cu_q, k_pages, v_pages, page_table, max_pages, num_pages,
+                            page_size, seq_lens, sink, o, workspace, workspace_bytes, B, Hq, Hkv,
+                            D, q_max, max_ctx, scale, ATTN_BF16, k_scale, v_scale, stream);
 }
 
 // ---------------------------------------------- GA verify without allocation

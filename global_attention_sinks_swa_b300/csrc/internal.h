@@ -56,6 +56,13 @@ cudaError_t launch_paged_append(const void *k_new, const void *v_new, const int3
                                 const int32_t *page_table, int max_pages, int num_pages,
                                 int page_size, int B, int Hkv, int D, int q_max, int elem_bytes,
                                 unsigned int *err, cudaStream_t s);
+// 8-bit paged append: bf16 new rows -> E4M3 codes of row / scale[kv head]
+// (fp32 division, round to nearest even, saturated at 448), D = 128.
+cudaError_t launch_paged_append_fp8(const void *k_new, const void *v_new, const int32_t *cu_q,
+                                    const int32_t *seq_lens, void *k_pages, void *v_pages,
+                                    const int32_t *page_table, int max_pages, int num_pages,
+                                    int page_size, const float *k_scale, const float *v_scale,
+                                    int B, int Hkv, int q_max, unsigned int *err, cudaStream_t s);
 
 // Verify (bf16, D = 128, mma.sync tensor cores, TMA-staged K/V).
 struct VerifyMaps {
@@ -83,7 +90,8 @@ cudaError_t launch_verify_paged(const VerifyMaps &maps, const void *q, const int
                                 const int32_t *seq_lens, const int32_t *page_table, int max_pages,
                                 int num_pages, const float *sink, void *o, float *ws_o,
                                 float *ws_ml, int nsplit, int B, int Hq, int Hkv, int q_max,
-                                int max_ctx, float scale, unsigned int *err, cudaStream_t s);
+                                int max_ctx, float scale, const float *k_scale,
+                                const float *v_scale, unsigned int *err, cudaStream_t s);
 
 // Index dumps.
 cudaError_t launch_debug_prefill_visits(int32_t *visits, int mode, int T, int window, int G,

@@ -299,6 +299,36 @@ ATTN_DEV void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// C[16x8] += A[16x16] * B[16x8], f16 inputs, fp32 accumulators.
+ATTN_DEV void mma_f16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------- 8-bit floats
+// Two E4M3 codes (low byte = first element) -> two f16 (low half = first);
+// exact: every E4M3 value is an f16 value.
+ATTN_DEV uint32_t e4m3x2_to_f16x2(uint16_t x) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(x));
+    return d;
+}
+// Two fp32 -> two E4M3 codes (first element in the low byte), round to
+// nearest even, finite values beyond 448 saturated.
+ATTN_DEV uint16_t f32x2_to_e4m3x2(float first, float second) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(second), "f"(first));
+    return d;
+}
+ATTN_DEV uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 // --------------------------------------------------------------------- math
 // 2^x on the SFU (approximate, flushes denormals; 2^-inf = 0).
 ATTN_DEV float exp2_approx(float x) {

@@ -18,6 +18,14 @@
 // O += PV and an online softmax in registers.  The two key halves merge in
 // shared memory; the sink logit joins the denominator once, in the final
 // merge (in-kernel for the ring, in the split combine for the paged cache).
+//
+// 8-bit paged cache (FP8 = true): pages hold E4M3 codes, entry = code * the
+// kv head's scale (K and V each have one), which halves the bytes read per
+// token.  TMA brings each 8 KB code block in; the two warps that share a key
+// half convert their 32 keys of K and of V to f16 (exact) in the 128-byte-
+// swizzled layout the bf16 path uses, and both products run as f16 mma.sync
+// (Q rounded to f16, P in f16).  The K scale folds into the score scale, the
+// V scale into the output.
 #include "index_math.cuh"
 #include "internal.h"
 #include "ptx_sm103.cuh"
@@ -36,6 +44,9 @@ constexpr unsigned kErrPage = 0x1u, kErrCtx = 0x2u, kErrQlen = 0x4u, kErrWait = 
 constexpr int kMergeStride = kD + 8;     // floats per row of the key-half merge buffer
 constexpr int kStageRowBytes = 2 * kD + 16;  // bytes per row of the bf16 output staging
 
+constexpr int kBlock8Bytes = kVerifyBlock * kD;  // one 8-bit block: 64 rows x 128 codes
+
+template <bool FP8>
 struct __align__(1024) VerifySmem {
     uint8_t k[kStages][2][kHalfBytes];  // after the loop: the key-half merge buffer
     uint8_t v[kStages][2][kHalfBytes];  // after the loop: the bf16 output staging
@@ -44,10 +55,32 @@ struct __align__(1024) VerifySmem {
     uint64_t empty[kStages];
     float merge_ml[2][16][2];
     int abort;
+    __device__ uint8_t *kt(int st, int hf) { return k[st][hf]; }  // 16-bit tiles computed on
+    __device__ uint8_t *vt(int st, int hf) { return v[st][hf]; }
+    __device__ float *merge() { return reinterpret_cast<float *>(k[0][0]); }
+    __device__ uint8_t *ostage() { return v[0][0]; }
+};
+template <>
+struct __align__(1024) VerifySmem<true> {
+    uint8_t k8[kStages][kBlock8Bytes];  // E4M3 code ring; after the loop: merge buffer
+    uint8_t v8[kStages][kBlock8Bytes];  // after the loop: the bf16 output staging
+    uint8_t k[2][kHalfBytes];           // f16 K and V of the block being computed
+    uint8_t v[2][kHalfBytes];
+    uint8_t q[2][kVerifyRows * 128];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    float merge_ml[2][16][2];
+    int abort;
+    __device__ uint8_t *kt(int, int hf) { return k[hf]; }
+    __device__ uint8_t *vt(int, int hf) { return v[hf]; }
+    __device__ float *merge() { return reinterpret_cast<float *>(k8[0]); }
+    __device__ uint8_t *ostage() { return v8[0]; }
 };
 
-static_assert(2 * 16 * kMergeStride * sizeof(float) <= sizeof(VerifySmem::k), "merge buffer");
-static_assert(kVerifyRows * kStageRowBytes <= sizeof(VerifySmem::v), "output staging");
+static_assert(2 * 16 * kMergeStride * sizeof(float) <= sizeof(VerifySmem<false>::k), "merge buffer");
+static_assert(kVerifyRows * kStageRowBytes <= sizeof(VerifySmem<false>::v), "output staging");
+static_assert(2 * 16 * kMergeStride * sizeof(float) <= sizeof(VerifySmem<true>::k8), "merge buffer");
+static_assert(kVerifyRows * kStageRowBytes <= sizeof(VerifySmem<true>::v8), "output staging");
 
 // Byte offset of element (row, d) inside a 128B-swizzled [rows][64] half tile;
 // d a multiple of 8.
@@ -70,6 +103,39 @@ struct KeySource {
     }
 };
 
+// Row r of an 8-bit [64][128] block (128-byte swizzle) -> f16 row r of the
+// two-half [64][64] layout (same swizzle), 16 codes at a time.
+__device__ __forceinline__ void fp8_row_to_f16(const uint8_t *src, uint8_t *dst0, uint8_t *dst1,
+                                               int r) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128 + (((c ^ r) & 7) << 4));
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w[2 * i] = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(xs[i] & 0xffffu));
+            w[2 * i + 1] = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(xs[i] >> 16));
+        }
+        uint8_t *half = (c < 4) ? dst0 : dst1;
+        const int d = (c & 3) * 16;
+        *reinterpret_cast<uint4 *>(half + sw128(r, d)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(half + sw128(r, d + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+template <bool FP8>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    if constexpr (FP8) ptx::mma_f16_16816(c, a, b0, b1);
+    else ptx::mma_bf16_16816(c, a, b0, b1);
+}
+template <bool FP8>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+    if constexpr (FP8) return ptx::pack_f16x2(lo, hi);
+    else return ptx::pack_bf16x2(lo, hi);
+}
+
 // Row-wise merge of two online-softmax states (log2 units): (m,l,o) <- (m,l,o) + (mb,lb,ob).
 __device__ __forceinline__ float merge_scale(float m, float mb, float *sa, float *sb) {
     const float mm = fmaxf(m, mb);
@@ -79,6 +145,7 @@ __device__ __forceinline__ float merge_scale(float m, float mb, float *sa, float
     return mm;
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 2)
     verify_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ cu_q,
@@ -86,9 +153,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                   int max_pages, int num_pages, const float *__restrict__ sink,
                   __nv_bfloat16 *__restrict__ o, float *__restrict__ ws_o,
                   float *__restrict__ ws_ml, int nsplit, int kind, int Hq, int Hkv, int window,
-                  int R, int q_max, int max_ctx, float scale, int finalize, unsigned *err) {
+                  int R, int q_max, int max_ctx, float scale, int finalize,
+                  const float *__restrict__ k_scale, const float *__restrict__ v_scale,
+                  unsigned *err) {
     extern __shared__ uint8_t smem_raw[];
-    VerifySmem &sm = *reinterpret_cast<VerifySmem *>(
+    VerifySmem<FP8> &sm = *reinterpret_cast<VerifySmem<FP8> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -161,13 +230,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
                     int c1, c2, c3;
                     if (kind == 0) { c1 = blk * kVerifyBlock; c2 = g; c3 = b; }
                     else           { c1 = 0;                  c2 = g; c3 = page; }
-                    for (int hf = 0; hf < 2; ++hf) {
-                        ptx::tma_load_4d(sm.k[st][hf], &tmk, hf * 64, c1, c2, c3, &sm.full[st]);
-                        ptx::tma_load_4d(sm.v[st][hf], &tmv, hf * 64, c1, c2, c3, &sm.full[st]);
+                    if constexpr (FP8) {  // one 8 KB box of codes each (128 codes per row)
+                        ptx::mbar_arrive_expect_tx(&sm.full[st], 2 * kBlock8Bytes);
+                        ptx::tma_load_4d(sm.k8[st], &tmk, 0, c1, c2, c3, &sm.full[st]);
+                        ptx::tma_load_4d(sm.v8[st], &tmv, 0, c1, c2, c3, &sm.full[st]);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(&sm.full[st], kStageBytes);
+                        for (int hf = 0; hf < 2; ++hf) {
+                            ptx::tma_load_4d(sm.k[st][hf], &tmk, hf * 64, c1, c2, c3, &sm.full[st]);
+                            ptx::tma_load_4d(sm.v[st][hf], &tmv, hf * 64, c1, c2, c3, &sm.full[st]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -185,6 +260,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (t < q_len)
             val = *reinterpret_cast<const uint4 *>(
                 q + (static_cast<long>(r0 + t) * Hq + g * G + hh) * kD + c * 8);
+        if constexpr (FP8) {  // bf16 -> f16 operands
+            const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&val);
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(p2[i]);
+                w[i] = ptx::pack_f16x2(f.x, f.y);
+            }
+            val = make_uint4(w[0], w[1], w[2], w[3]);
+        }
         *reinterpret_cast<uint4 *>(sm.q[c >> 3] + sw128(r, (c & 7) * 8)) = val;
     }
     ptx::named_bar_sync(1, kConsumers * 32);
@@ -208,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         qpos[h2] = (t < q_len) ? L - q_len + t : -1;
     }
     const int win = (kind == 0) ? window : 0;
-    const float sl2 = scale * kLog2e;
+    const float sl2 = scale * kLog2e * (FP8 ? k_scale[g] : 1.f);  // the K scale joins the score scale
 
     float oacc[16][4];
 #pragma unroll
@@ -217,10 +302,24 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     for (int blk = 0; blk < nblk; ++blk) {
         const int st = blk % kStages;
-        if (!ptx::mbar_wait(&sm.full[st], (blk / kStages) & 1)) {
+        bool landed = ptx::mbar_wait(&sm.full[st], (blk / kStages) & 1);
+        if constexpr (FP8) {
+            // the pair of warps on this key half decides together (and both
+            // are done with the previous block's f16 rows past this barrier)
+            landed = !ptx::named_bar_or(2 + kh, 64, !landed);
+        }
+        if (!landed) {
             if (lane == 0) atomicOr(err, kErrWait);
             sm.abort = 1;
             break;
+        }
+        if constexpr (FP8) {  // warp mt = 0 converts the half's K rows, mt = 1 its V rows
+            const int r = kh * 32 + lane;
+            if (mt == 0) fp8_row_to_f16(sm.k8[st], sm.k[0], sm.k[1], r);
+            else fp8_row_to_f16(sm.v8[st], sm.v[0], sm.v[1], r);
+            ptx::named_bar_sync(2 + kh, 64);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.empty[st]);  // the codes are no longer needed
         }
         // ring: a warp whose 32 keys of this block all lie past the last slot skips it
         if (active && (kind != 0 || blk * kVerifyBlock + kh * 32 < R)) {
@@ -232,14 +331,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const int d = kk * 16 + (mi & 1) * 8;
-                const uint32_t kbase = ptx::smem_u32(sm.k[st][d >> 6]);
+                const uint32_t kbase = ptx::smem_u32(sm.kt(st, d >> 6));
 #pragma unroll
                 for (int np = 0; np < 2; ++np) {
                     const int key = kh * 32 + np * 16 + (mi >> 1) * 8 + (lane & 7);
                     uint32_t b0, b1, b2, b3;
                     ptx::ldsm_x4(kbase + sw128(key, d & 63), b0, b1, b2, b3);
-                    ptx::mma_bf16_16816(s[2 * np], qf[kk], b0, b1);
-                    ptx::mma_bf16_16816(s[2 * np + 1], qf[kk], b2, b3);
+                    mma16816<FP8>(s[2 * np], qf[kk], b0, b1);
+                    mma16816<FP8>(s[2 * np + 1], qf[kk], b2, b3);
                 }
             }
             // mask, scale to log2 units, online softmax
@@ -284,24 +383,24 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int k2 = 0; k2 < 2; ++k2) {
                 uint32_t pa[4];
-                pa[0] = ptx::pack_bf16x2(s[2 * k2][0], s[2 * k2][1]);
-                pa[1] = ptx::pack_bf16x2(s[2 * k2][2], s[2 * k2][3]);
-                pa[2] = ptx::pack_bf16x2(s[2 * k2 + 1][0], s[2 * k2 + 1][1]);
-                pa[3] = ptx::pack_bf16x2(s[2 * k2 + 1][2], s[2 * k2 + 1][3]);
+                pa[0] = pack16<FP8>(s[2 * k2][0], s[2 * k2][1]);
+                pa[1] = pack16<FP8>(s[2 * k2][2], s[2 * k2][3]);
+                pa[2] = pack16<FP8>(s[2 * k2 + 1][0], s[2 * k2 + 1][1]);
+                pa[3] = pack16<FP8>(s[2 * k2 + 1][2], s[2 * k2 + 1][3]);
                 const int key = kh * 32 + k2 * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
                 for (int nd = 0; nd < 8; ++nd) {
                     const int d = nd * 16 + (mi >> 1) * 8;
                     uint32_t b0, b1, b2, b3;
-                    ptx::ldsm_x4_t(ptx::smem_u32(sm.v[st][d >> 6]) + sw128(key, d & 63), b0, b1,
+                    ptx::ldsm_x4_t(ptx::smem_u32(sm.vt(st, d >> 6)) + sw128(key, d & 63), b0, b1,
                                    b2, b3);
-                    ptx::mma_bf16_16816(oacc[2 * nd], pa, b0, b1);
-                    ptx::mma_bf16_16816(oacc[2 * nd + 1], pa, b2, b3);
+                    mma16816<FP8>(oacc[2 * nd], pa, b0, b1);
+                    mma16816<FP8>(oacc[2 * nd + 1], pa, b2, b3);
                 }
             }
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.empty[st]);
+        if (!FP8 && lane == 0) ptx::mbar_arrive(&sm.empty[st]);
     }
 
     // ---- merge the two key halves (warp kh=1 -> smem -> warp kh=0)
@@ -312,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     ptx::named_bar_sync(1, kConsumers * 32);  // every warp is done with the stage buffers
     // rows padded to kMergeStride floats: float2 writes of 8 rows hit distinct banks
-    float *mo = reinterpret_cast<float *>(sm.k[0][0]) + mt * 16 * kMergeStride;
+    float *mo = sm.merge() + mt * 16 * kMergeStride;
     if (kh == 1 && active) {
 #pragma unroll
         for (int n = 0; n < 16; ++n)
@@ -354,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (finalize) {
         // add the sink once; bf16 rows staged in shared memory (rows padded to
         // kStageRowBytes), then written with coalesced 16-byte stores
-        uint8_t *ost = sm.v[0][0];
+        uint8_t *ost = sm.ostage();
         if (lead) {
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -369,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     float ssa, ssb;
                     merge_scale(mrow[h2], s2, &ssa, &ssb);
                     const float z = lrow[h2] * ssa + ssb;
-                    inv = ssa / z;
+                    inv = ssa / z * (FP8 ? v_scale[g] : 1.f);  // the V scale joins the output
                 }
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
@@ -402,11 +501,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 wml[r * 2 + 0] = mrow[h2];
                 wml[r * 2 + 1] = lrow[h2];
             }
+            const float vs = FP8 ? v_scale[g] : 1.f;  // the V scale joins the output
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
                 const int d = n * 8 + 2 * (lane & 3);
                 *reinterpret_cast<float2 *>(wo + r * kD + d) =
-                    make_float2(oacc[n][2 * h2], oacc[n][2 * h2 + 1]);
+                    make_float2(oacc[n][2 * h2] * vs, oacc[n][2 * h2 + 1] * vs);
             }
         }
     }
@@ -466,7 +566,8 @@ __global__ void __launch_bounds__(256)
         *reinterpret_cast<uint32_t *>(orow + d) = ptx::pack_bf16x2(acc[d] * inv, acc[d + 1] * inv);
 }
 
-size_t verify_smem_bytes() { return sizeof(VerifySmem) + 1024; }
+template <bool FP8>
+size_t verify_smem_bytes() { return sizeof(VerifySmem<FP8>) + 1024; }
 
 }  // namespace
 
@@ -475,14 +576,15 @@ cudaError_t launch_verify_ring(const VerifyMaps &maps, const void *q, const int3
                                int Hkv, int window, int R, int q_max, float scale,
                                unsigned int *err, cudaStream_t s) {
     if (B == 0) return cudaSuccess;
-    const size_t smem = verify_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = verify_smem_bytes<false>();
+    cudaError_t e = cudaFuncSetAttribute(verify_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    verify_kernel<<<dim3(1, Hkv, B), kThreads, smem, s>>>(
+    verify_kernel<false><<<dim3(1, Hkv, B), kThreads, smem, s>>>(
         maps.k, maps.v, static_cast<const __nv_bfloat16 *>(q), cu_q, seq_lens, nullptr, 0, 0, sink,
         static_cast<__nv_bfloat16 *>(o), nullptr, nullptr, 1, 0, Hq, Hkv, window, R, q_max, 0,
-        scale, 1, err);
+        scale, 1, nullptr, nullptr, err);
     return cudaGetLastError();
 }
 
@@ -490,17 +592,20 @@ cudaError_t launch_verify_paged(const VerifyMaps &maps, const void *q, const int
                                 const int32_t *seq_lens, const int32_t *page_table, int max_pages,
                                 int num_pages, const float *sink, void *o, float *ws_o,
                                 float *ws_ml, int nsplit, int B, int Hq, int Hkv, int q_max,
-                                int max_ctx, float scale, unsigned int *err, cudaStream_t s) {
+                                int max_ctx, float scale, const float *k_scale,
+                                const float *v_scale, unsigned int *err, cudaStream_t s) {
     if (B == 0) return cudaSuccess;
-    const size_t smem = verify_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool fp8 = k_scale != nullptr;
+    const size_t smem = fp8 ? verify_smem_bytes<true>() : verify_smem_bytes<false>();
+    auto kern = fp8 ? verify_kernel<true> : verify_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int finalize = (nsplit == 1) ? 1 : 0;
-    verify_kernel<<<dim3(nsplit, Hkv, B), kThreads, smem, s>>>(
+    kern<<<dim3(nsplit, Hkv, B), kThreads, smem, s>>>(
         maps.k, maps.v, static_cast<const __nv_bfloat16 *>(q), cu_q, seq_lens, page_table,
         max_pages, num_pages, sink, static_cast<__nv_bfloat16 *>(o), ws_o, ws_ml, nsplit, 1, Hq,
-        Hkv, 0, 0, q_max, max_ctx, scale, finalize, err);
+        Hkv, 0, 0, q_max, max_ctx, scale, finalize, k_scale, v_scale, err);
     e = cudaGetLastError();
     if (e != cudaSuccess || finalize) return e;
     verify_combine_kernel<<<dim3(Hkv, B), 256, 0, s>>>(ws_o, ws_ml, cu_q, seq_lens, sink,

@@ -25,6 +25,11 @@
  *   [SERVE]  summary section "MTP加速": serving measured with 16K-token prompts
  *            at several in-node batch sizes (batches of prompts of unequal
  *            length, packed here by cu_seqlens).
+ *   [FP8]    technical-report summary, section "MiMo-V2-Flash Model Architecture":
+ *            an FP8 mixed-precision framework; dpshk.com article, section
+ *            "关键配置参数": FP8 quantization enabled at inference to cut memory.
+ *            Verify is bound by reading the cache, so 8-bit GA pages halve the
+ *            bytes of a verify step.
  *   [CFG]    dpshk.com article on MiMo-V2-Flash-Base ("小米AI团队揭秘"), section
  *            "轻量级多token预测技术": config.json lists attention_value_scale =
  *            0.707 without saying what it scales; read here as a factor on the
@@ -160,6 +165,20 @@ attn_status_t attn_ga_paged_append(const void *k_new, const void *v_new, const i
                                    int page_size, int B, int Hkv, int D, int q_max,
                                    attn_dtype_t dtype, void *stream);
 
+/* 8-bit GA paged cache [FP8]: k_pages, v_pages [num_pages,Hkv,page_size,D]
+ * uint8 E4M3 codes (sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; largest finite 448); entry = code * k_scale[g] (v_scale[g] for
+ * V), k_scale/v_scale [Hkv] fp32 on the device, chosen by the caller.  The
+ * append takes bf16 k_new/v_new [cu_q[B],Hkv,D] and stores the code of
+ * value / scale (fp32 division, round to nearest even, finite values beyond
+ * 448 saturated).  D = 128; errors as for attn_ga_paged_append. */
+attn_status_t attn_ga_paged_append_fp8(const void *k_new, const void *v_new,
+                                       const int32_t *cu_q, const int32_t *seq_lens,
+                                       void *k_pages, void *v_pages, const int32_t *page_table,
+                                       int max_pages, int num_pages, int page_size,
+                                       const float *k_scale, const float *v_scale, int B, int Hkv,
+                                       int D, int q_max, void *stream);
+
 /* ----------------------------------------------------------------- verify ---
  * MTP verify [MTP]: request b scores its q_len = cu_q[b+1]-cu_q[b] <= q_max
  * new tokens (positions seq_lens[b]-q_len .. seq_lens[b]-1, already appended)
@@ -190,6 +209,20 @@ attn_status_t attn_ga_sink_verify(const void *q, const int32_t *cu_q, const void
                                   size_t workspace_bytes, int B, int Hq, int Hkv, int D,
                                   int q_max, int max_ctx, float scale, attn_dtype_t dtype,
                                   void *stream);
+
+/* GA verify over the 8-bit paged cache [FP8] (layout and scales as for
+ * attn_ga_paged_append_fp8): half the cache bytes of attn_ga_sink_verify per
+ * token.  q and o bf16; the codes become f16 exactly, and both products run
+ * with f16 operands (q rounded to f16, so |q| must stay below 65504) and
+ * fp32 accumulation.  Workspace, sizes and errors as attn_ga_sink_verify. */
+attn_status_t attn_ga_sink_verify_fp8(const void *q, const int32_t *cu_q, const void *k_pages,
+                                      const void *v_pages, const int32_t *page_table,
+                                      int max_pages, int num_pages, int page_size,
+                                      const int32_t *seq_lens, const float *sink,
+                                      const float *k_scale, const float *v_scale, void *o,
+                                      void *workspace, size_t workspace_bytes, int B, int Hq,
+                                      int Hkv, int D, int q_max, int max_ctx, float scale,
+                                      void *stream);
 
 /* The same GA verify for callers that cannot allocate device memory (for
  * example code inside a host program that reserved all device memory up front

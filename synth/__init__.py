@@ -28,6 +28,20 @@ def normal(shape, seed: int, dtype=torch.bfloat16, device="cpu") -> torch.Tensor
     return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(dtype)
 
 
+def e4m3_codes(shape, seed: int, per_unit: float = 50.0, device="cpu") -> torch.Tensor:
+    """uint8 E4M3 codes of N(0,1) * per_unit draws (torch's float8_e4m3fn cast,
+    a library routine; draws clamped to the finite range first): an 8-bit
+    cache whose entries, times a scale of about 1/per_unit, are ~ N(0,1)."""
+    x = normal(shape, seed, torch.float32, device) * per_unit
+    return x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def kv_scales(Hkv: int, seed: int, device="cpu") -> torch.Tensor:
+    """Per-kv-head fp32 cache scales, uniform in [0.01, 0.03]."""
+    g = _gen(seed, device)
+    return 0.01 + 0.02 * torch.rand(Hkv, generator=g, device=device)
+
+
 def prefill_inputs(B: int, T: int, Hq: int, Hkv: int, D: int, seed: int,
                    dtype=torch.bfloat16, device="cpu"):
     """q [B,T,Hq,D], k/v [B,T,Hkv,D] in `dtype`; sink [Hq] fp32."""
