@@ -21,11 +21,19 @@
 //
 // 8-bit paged cache (FP8 = true): pages hold E4M3 codes, entry = code * the
 // kv head's scale (K and V each have one), which halves the bytes read per
-// token.  TMA brings each 8 KB code block in; the two warps that share a key
-// half convert their 32 keys of K and of V to f16 (exact) in the 128-byte-
-// swizzled layout the bf16 path uses, and both products run as f16 mma.sync
-// (Q rounded to f16, P in f16).  The K scale folds into the score scale, the
-// V scale into the output.
+// token.  TMA brings 8 KB code blocks into a deeper ring (the same bytes in
+// flight as the bf16 ring), and the codes go from shared memory straight into
+// f16 mma.sync fragments (cvt.f16x2.e4m3x2 is exact), with Q rounded to f16
+// and P in f16:
+//   K: ldmatrix of 16-byte code rows gives a thread 4 consecutive d of one
+//      key; fragment k positions {2c,2c+1 | 2c+8,2c+9} are taken to mean d
+//      {4c,4c+1 | 4c+2,4c+3} of the 16-d chunk, and Q is loaded with the
+//      same order (the sum over d does not care);
+//   V: ldmatrix.trans gives two keys x two adjacent d; byte permutes split
+//      them into an "even d" and an "odd d" fragment, so O tile 2j holds
+//      d = 16j + 2n and tile 2j+1 holds d = 16j + 2n + 1: a thread's four
+//      accumulators of a row are four consecutive d.
+// The K scale folds into the score scale, the V scale into the output.
 #include "index_math.cuh"
 #include "internal.h"
 #include "ptx_sm103.cuh"
@@ -45,6 +53,8 @@ constexpr int kMergeStride = kD + 8;     // floats per row of the key-half merge
 constexpr int kStageRowBytes = 2 * kD + 16;  // bytes per row of the bf16 output staging
 
 constexpr int kBlock8Bytes = kVerifyBlock * kD;  // one 8-bit block: 64 rows x 128 codes
+template <bool FP8>
+constexpr int kStagesOf = FP8 ? 2 * kStages : kStages;  // the same bytes in flight
 
 template <bool FP8>
 struct __align__(1024) VerifySmem {
@@ -62,17 +72,13 @@ struct __align__(1024) VerifySmem {
 };
 template <>
 struct __align__(1024) VerifySmem<true> {
-    uint8_t k8[kStages][kBlock8Bytes];  // E4M3 code ring; after the loop: merge buffer
-    uint8_t v8[kStages][kBlock8Bytes];  // after the loop: the bf16 output staging
-    uint8_t k[2][kHalfBytes];           // f16 K and V of the block being computed
-    uint8_t v[2][kHalfBytes];
-    uint8_t q[2][kVerifyRows * 128];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint8_t k8[kStagesOf<true>][kBlock8Bytes];  // E4M3 code ring; after the loop: merge buffer
+    uint8_t v8[kStagesOf<true>][kBlock8Bytes];  // after the loop: the bf16 output staging
+    uint8_t q[2][kVerifyRows * 128];             // Q in f16
+    uint64_t full[kStagesOf<true>];
+    uint64_t empty[kStagesOf<true>];
     float merge_ml[2][16][2];
     int abort;
-    __device__ uint8_t *kt(int, int hf) { return k[hf]; }
-    __device__ uint8_t *vt(int, int hf) { return v[hf]; }
     __device__ float *merge() { return reinterpret_cast<float *>(k8[0]); }
     __device__ uint8_t *ostage() { return v8[0]; }
 };
@@ -103,25 +109,28 @@ struct KeySource {
     }
 };
 
-// Row r of an 8-bit [64][128] block (128-byte swizzle) -> f16 row r of the
-// two-half [64][64] layout (same swizzle), 16 codes at a time.
-__device__ __forceinline__ void fp8_row_to_f16(const uint8_t *src, uint8_t *dst0, uint8_t *dst1,
-                                               int r) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128 + (((c ^ r) & 7) << 4));
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            w[2 * i] = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(xs[i] & 0xffffu));
-            w[2 * i + 1] = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(xs[i] >> 16));
-        }
-        uint8_t *half = (c < 4) ? dst0 : dst1;
-        const int d = (c & 3) * 16;
-        *reinterpret_cast<uint4 *>(half + sw128(r, d)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4 *>(half + sw128(r, d + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
-    }
+// Output accumulators as 16 pairs (x, y) = O[row][d], O[row][d+1] per row half
+// h2 of a thread: bf16 path, tile i holds d = 8i + 2c, +1; 8-bit path, tiles
+// 2j / 2j+1 hold the even / odd d of chunk j, pair i = (j, e) is d = 16j+4c+2e.
+template <bool FP8>
+__device__ __forceinline__ float &acc_x(float (&o)[16][4], int i, int h2) {
+    if constexpr (FP8) return o[2 * (i >> 1)][2 * h2 + (i & 1)];
+    else return o[i][2 * h2];
+}
+template <bool FP8>
+__device__ __forceinline__ float &acc_y(float (&o)[16][4], int i, int h2) {
+    if constexpr (FP8) return o[2 * (i >> 1) + 1][2 * h2 + (i & 1)];
+    else return o[i][2 * h2 + 1];
+}
+template <bool FP8>
+__device__ __forceinline__ int acc_d(int i, int c) {
+    if constexpr (FP8) return 16 * (i >> 1) + 4 * c + 2 * (i & 1);
+    else return 8 * i + 2 * c;
+}
+
+// Two E4M3 codes (bytes lo, hi of x) -> f16x2 B operand.
+__device__ __forceinline__ uint32_t codes_f16x2(uint32_t x, uint32_t sel) {
+    return ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(x, 0u, sel) & 0xffffu));
 }
 
 template <bool FP8>
@@ -191,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         nblk = pe - pb;
     }
 
+    constexpr int kS = kStagesOf<FP8>;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kS; ++s) {
             ptx::mbar_init(&sm.full[s], 1);
             ptx::mbar_init(&sm.empty[s], kConsumers);
         }
@@ -222,9 +232,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < n; ++j) {
                 const int blk = base + j;
                 const int page = __shfl_sync(0xffffffffu, my_page, j);
-                const int st = blk % kStages;
-                if (blk >= kStages) {
-                    if (!ptx::mbar_wait_warp(&sm.empty[st], ((blk / kStages) - 1) & 1)) {
+                const int st = blk % kS;
+                if (blk >= kS) {
+                    if (!ptx::mbar_wait_warp(&sm.empty[st], ((blk / kS) - 1) & 1)) {
                         if (lane == 0) atomicOr(err, kErrWait);
                         return;
                     }
@@ -278,11 +288,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool active = mt * 16 < q_len * G;  // this warp's rows hold real queries
     uint32_t qf[8][4];
     if (active) {
-        const int row = mt * 16 + (lane & 15);
-        for (int kk = 0; kk < 8; ++kk) {
-            const int d = kk * 16 + (lane >> 4) * 8;
-            ptx::ldsm_x4(ptx::smem_u32(sm.q[d >> 6]) + sw128(row, d & 63), qf[kk][0], qf[kk][1],
-                         qf[kk][2], qf[kk][3]);
+        if constexpr (FP8) {  // k positions {2c,2c+1 | 2c+8,2c+9} = d {4c,4c+1 | 4c+2,4c+3}
+            const int c = lane & 3;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int d = kk * 16 + 4 * c;
+                const uint8_t *half = sm.q[d >> 6];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int row = mt * 16 + (lane >> 2) + 8 * h2;
+                    const uint8_t *p = half + sw128(row, d & 56) + (d & 7) * 2;
+                    qf[kk][h2] = *reinterpret_cast<const uint32_t *>(p);
+                    qf[kk][2 + h2] = *reinterpret_cast<const uint32_t *>(p + 4);
+                }
+            }
+        } else {
+            const int row = mt * 16 + (lane & 15);
+            for (int kk = 0; kk < 8; ++kk) {
+                const int d = kk * 16 + (lane >> 4) * 8;
+                ptx::ldsm_x4(ptx::smem_u32(sm.q[d >> 6]) + sw128(row, d & 63), qf[kk][0],
+                             qf[kk][1], qf[kk][2], qf[kk][3]);
+            }
         }
     }
     // query positions of this thread's two rows (-1: padding row, sees nothing)
@@ -301,25 +327,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
     for (int blk = 0; blk < nblk; ++blk) {
-        const int st = blk % kStages;
-        bool landed = ptx::mbar_wait(&sm.full[st], (blk / kStages) & 1);
-        if constexpr (FP8) {
-            // the pair of warps on this key half decides together (and both
-            // are done with the previous block's f16 rows past this barrier)
-            landed = !ptx::named_bar_or(2 + kh, 64, !landed);
-        }
-        if (!landed) {
+        const int st = blk % kS;
+        if (!ptx::mbar_wait(&sm.full[st], (blk / kS) & 1)) {
             if (lane == 0) atomicOr(err, kErrWait);
             sm.abort = 1;
             break;
-        }
-        if constexpr (FP8) {  // warp mt = 0 converts the half's K rows, mt = 1 its V rows
-            const int r = kh * 32 + lane;
-            if (mt == 0) fp8_row_to_f16(sm.k8[st], sm.k[0], sm.k[1], r);
-            else fp8_row_to_f16(sm.v8[st], sm.v[0], sm.v[1], r);
-            ptx::named_bar_sync(2 + kh, 64);
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sm.empty[st]);  // the codes are no longer needed
         }
         // ring: a warp whose 32 keys of this block all lie past the last slot skips it
         if (active && (kind != 0 || blk * kVerifyBlock + kh * 32 < R)) {
@@ -328,17 +340,32 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
             const int mi = lane >> 3;
+            if constexpr (FP8) {
+                // one ldmatrix per 16-d chunk: matrix j = keys 8j..8j+7 of this half
+                const int key = kh * 32 + 8 * mi + (lane & 7);
+                const uint32_t krow = ptx::smem_u32(sm.k8[st]) + key * 128;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const int d = kk * 16 + (mi & 1) * 8;
-                const uint32_t kbase = ptx::smem_u32(sm.kt(st, d >> 6));
+                for (int kk = 0; kk < 8; ++kk) {
+                    uint32_t r[4];
+                    ptx::ldsm_x4(krow + (((kk ^ key) & 7) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    const int key = kh * 32 + np * 16 + (mi >> 1) * 8 + (lane & 7);
-                    uint32_t b0, b1, b2, b3;
-                    ptx::ldsm_x4(kbase + sw128(key, d & 63), b0, b1, b2, b3);
-                    mma16816<FP8>(s[2 * np], qf[kk], b0, b1);
-                    mma16816<FP8>(s[2 * np + 1], qf[kk], b2, b3);
+                    for (int j = 0; j < 4; ++j)
+                        mma16816<true>(s[j], qf[kk], codes_f16x2(r[j], 0x10u),
+                                       codes_f16x2(r[j], 0x32u));
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int d = kk * 16 + (mi & 1) * 8;
+                    const uint32_t kbase = ptx::smem_u32(sm.k[st][d >> 6]);
+#pragma unroll
+                    for (int np = 0; np < 2; ++np) {
+                        const int key = kh * 32 + np * 16 + (mi >> 1) * 8 + (lane & 7);
+                        uint32_t b0, b1, b2, b3;
+                        ptx::ldsm_x4(kbase + sw128(key, d & 63), b0, b1, b2, b3);
+                        mma16816<false>(s[2 * np], qf[kk], b0, b1);
+                        mma16816<false>(s[2 * np + 1], qf[kk], b2, b3);
+                    }
                 }
             }
             // mask, scale to log2 units, online softmax
@@ -388,19 +415,38 @@ __global__ void __launch_bounds__(kThreads, 2)
                 pa[2] = pack16<FP8>(s[2 * k2 + 1][0], s[2 * k2 + 1][1]);
                 pa[3] = pack16<FP8>(s[2 * k2 + 1][2], s[2 * k2 + 1][3]);
                 const int key = kh * 32 + k2 * 16 + (mi & 1) * 8 + (lane & 7);
+                if constexpr (FP8) {
+                    // matrices: keys 0-7 / 8-15 of this chunk x d-chunks 2dp, 2dp+1
+                    const uint32_t vrow = ptx::smem_u32(sm.v8[st]) + key * 128;
 #pragma unroll
-                for (int nd = 0; nd < 8; ++nd) {
-                    const int d = nd * 16 + (mi >> 1) * 8;
-                    uint32_t b0, b1, b2, b3;
-                    ptx::ldsm_x4_t(ptx::smem_u32(sm.vt(st, d >> 6)) + sw128(key, d & 63), b0, b1,
-                                   b2, b3);
-                    mma16816<FP8>(oacc[2 * nd], pa, b0, b1);
-                    mma16816<FP8>(oacc[2 * nd + 1], pa, b2, b3);
+                    for (int dp = 0; dp < 4; ++dp) {
+                        const int dch = 2 * dp + (mi >> 1);
+                        uint32_t r[4];
+                        ptx::ldsm_x4_t(vrow + (((dch ^ key) & 7) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {  // d-chunk 2dp + h: registers 2h, 2h+1
+                            const int nd = 2 * dp + h;
+                            mma16816<true>(oacc[2 * nd], pa, codes_f16x2(r[2 * h], 0x20u),
+                                           codes_f16x2(r[2 * h + 1], 0x20u));
+                            mma16816<true>(oacc[2 * nd + 1], pa, codes_f16x2(r[2 * h], 0x31u),
+                                           codes_f16x2(r[2 * h + 1], 0x31u));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int nd = 0; nd < 8; ++nd) {
+                        const int d = nd * 16 + (mi >> 1) * 8;
+                        uint32_t b0, b1, b2, b3;
+                        ptx::ldsm_x4_t(ptx::smem_u32(sm.v[st][d >> 6]) + sw128(key, d & 63), b0,
+                                       b1, b2, b3);
+                        mma16816<false>(oacc[2 * nd], pa, b0, b1);
+                        mma16816<false>(oacc[2 * nd + 1], pa, b2, b3);
+                    }
                 }
             }
         }
         __syncwarp();
-        if (!FP8 && lane == 0) ptx::mbar_arrive(&sm.empty[st]);
+        if (lane == 0) ptx::mbar_arrive(&sm.empty[st]);
     }
 
     // ---- merge the two key halves (warp kh=1 -> smem -> warp kh=0)
@@ -417,9 +463,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int n = 0; n < 16; ++n)
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-                const int rr = (lane >> 2) + h2 * 8, d = n * 8 + 2 * (lane & 3);
+                const int rr = (lane >> 2) + h2 * 8, d = acc_d<FP8>(n, lane & 3);
                 *reinterpret_cast<float2 *>(mo + rr * kMergeStride + d) =
-                    make_float2(oacc[n][2 * h2], oacc[n][2 * h2 + 1]);
+                    make_float2(acc_x<FP8>(oacc, n, h2), acc_y<FP8>(oacc, n, h2));
             }
         if ((lane & 3) == 0)
             for (int h2 = 0; h2 < 2; ++h2) {
@@ -443,10 +489,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int n = 0; n < 16; ++n)
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-                const int rr = (lane >> 2) + h2 * 8, d = n * 8 + 2 * (lane & 3);
+                const int rr = (lane >> 2) + h2 * 8, d = acc_d<FP8>(n, lane & 3);
                 const float2 x = *reinterpret_cast<const float2 *>(mo + rr * kMergeStride + d);
-                oacc[n][2 * h2] = oacc[n][2 * h2] * sa[h2] + x.x * sb[h2];
-                oacc[n][2 * h2 + 1] = oacc[n][2 * h2 + 1] * sa[h2] + x.y * sb[h2];
+                float &ax = acc_x<FP8>(oacc, n, h2), &ay = acc_y<FP8>(oacc, n, h2);
+                ax = ax * sa[h2] + x.x * sb[h2];
+                ay = ay * sa[h2] + x.y * sb[h2];
             }
     }
 
@@ -472,9 +519,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
-                    const int d = n * 8 + 2 * (lane & 3);
+                    const int d = acc_d<FP8>(n, lane & 3);
                     *reinterpret_cast<uint32_t *>(ost + r * kStageRowBytes + d * 2) =
-                        ptx::pack_bf16x2(oacc[n][2 * h2] * inv, oacc[n][2 * h2 + 1] * inv);
+                        ptx::pack_bf16x2(acc_x<FP8>(oacc, n, h2) * inv, acc_y<FP8>(oacc, n, h2) * inv);
                 }
             }
         }
@@ -504,9 +551,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float vs = FP8 ? v_scale[g] : 1.f;  // the V scale joins the output
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
-                const int d = n * 8 + 2 * (lane & 3);
+                const int d = acc_d<FP8>(n, lane & 3);
                 *reinterpret_cast<float2 *>(wo + r * kD + d) =
-                    make_float2(oacc[n][2 * h2] * vs, oacc[n][2 * h2 + 1] * vs);
+                    make_float2(acc_x<FP8>(oacc, n, h2) * vs, acc_y<FP8>(oacc, n, h2) * vs);
             }
         }
     }
