@@ -316,6 +316,13 @@ ATTN_DEV uint32_t e4m3x2_to_f16x2(uint16_t x) {
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(x));
     return d;
 }
+// Four E4M3 codes (bytes 0..3 of x) -> f16x2 of bytes 0,1 and of bytes 2,3.
+ATTN_DEV void e4m3x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
 // Two fp32 -> two E4M3 codes (first element in the low byte), round to
 // nearest even, finite values beyond 448 saturated.
 ATTN_DEV uint16_t f32x2_to_e4m3x2(float first, float second) {

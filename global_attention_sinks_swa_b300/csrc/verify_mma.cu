@@ -349,9 +349,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                     uint32_t r[4];
                     ptx::ldsm_x4(krow + (((kk ^ key) & 7) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma16816<true>(s[j], qf[kk], codes_f16x2(r[j], 0x10u),
-                                       codes_f16x2(r[j], 0x32u));
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t b0, b1;
+                        ptx::e4m3x4_to_f16x2x2(r[j], b0, b1);
+                        mma16816<true>(s[j], qf[kk], b0, b1);
+                    }
                 }
             } else {
 #pragma unroll
