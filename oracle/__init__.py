@@ -14,6 +14,8 @@ Contents
   column, a library softmax) used to pin the C code on tiny inputs.
 - ``index``: the integer definitions the kernels' index arithmetic must
   reproduce bit for bit (visibility, ring slot, page location).
+- ``backward``: gradients dq, dk, dv and the sink's dsigma by the softmax
+  Jacobian written out in fp64.
 - ``fp8``: the E4M3 codes of an 8-bit KV cache (decode, encode with
   round-to-nearest-even and saturation, per-kv-head scales); ``verify_fp8``
   is ``verify`` over the dequantized history.
@@ -34,7 +36,7 @@ import threading
 
 import numpy as np
 
-from . import brute, fp8, index  # noqa: F401  (re-exported)
+from . import backward, brute, fp8, index  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_sink_oracle.c")
