@@ -313,6 +313,30 @@ def bench_prefill_packed(A, synth, steps: int, warmup: int, world: int, stream, 
     return ms, flop, nbytes, lens
 
 
+def bench_backward(A, synth, steps: int, warmup: int, world: int, stream, seed: int):
+    """SWA backward (dq, dk, dv, dsink) at the headline sizes; FLOP = the five
+    products over visible pairs (S, dP, dV, dK, dQ): 10*D*Hq per pair."""
+    import torch
+    q, k, v, sink = synth.prefill_inputs(B, T, HQ, HKV, D, seed, device="cuda")
+    dout = synth.normal((B, T, HQ, D), seed + 1, device="cuda")
+    lse = torch.empty(B, HQ, T, device="cuda")
+    o = A.attn_swa_sink_prefill(q, k, v, sink, window=W, lse=lse, stream=stream)
+    ws = torch.empty(A._lib.attn_sink_prefill_backward_workspace(B, T, HQ, D), dtype=torch.uint8,
+                     device="cuda")
+
+    def step(_):
+        A.attn_sink_prefill_backward(q, k, v, o, lse, dout, sink, window=W, workspace=ws,
+                                     stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+        ms = time_region(step, steps, world, stream)
+    if A.attn_check_device_error(stream) != 0:
+        raise RuntimeError("backward reported a device error")
+    return ms, 10.0 * D * HQ * visible_pairs(T, W) * B
+
+
 def bench_prefill_e2e(A, synth, steps: int, warmup: int, world: int, stream, seed: int):
     """Same metric through the public call with host buffers: every step
     copies its inputs (q, k, v, sink) from pinned host memory and its output
@@ -546,6 +570,14 @@ def main():
             "roofline": {"bound": "hbm", "achieved": bytes_pk / (ms_pk * 1e-3) / 1e9,
                          "peak": hbm, "unit": "GB/s",
                          "frac": bytes_pk / (ms_pk * 1e-3) / 1e9 / hbm}}
+        ms_bw, flop_bw = bench_backward(A, synth, max(3, steps_p // 2), warmup, world, stream,
+                                        1008 + 10 * rank)
+        parts["swa_backward"] = {
+            "config": "B=1 T=32768 Hq=64 Hkv=8 D=128 W=128 bf16: dq, dk, dv, dsink",
+            "value": flop_bw / (ms_bw * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms_bw,
+            "flop": "10*D*Hq per visible pair (five products)",
+            "roofline": {"bound": "tensor", "peak": tf_burst, "unit": "TFLOP/s",
+                         "frac": flop_bw / (ms_bw * 1e-3) / 1e12 / tf_burst}}
         ctx4 = synth.context_lengths(64, 4096, 65536, 1004)
         ms4, kv4 = bench_verify_ga(A, ctx4, np.full(64, QMAX, np.int32), args.steps, warmup, world,
                                    stream, 1004 + 10 * rank)

@@ -46,6 +46,8 @@ _SIGS = {
     "attn_check_device_error": ([_vp, ctypes.POINTER(ctypes.c_uint)], _ci),
     "attn_swa_sink_prefill": ([_vp] * 6 + [_ci] * 6 + [_cf, _ci, _vp], _ci),
     "attn_ga_sink_prefill": ([_vp] * 6 + [_ci] * 5 + [_cf, _ci, _vp], _ci),
+    "attn_sink_prefill_backward_workspace": ([_ci] * 4, _sz),
+    "attn_sink_prefill_backward": ([_vp] * 12 + [_sz] + [_ci] * 6 + [_cf, _ci, _vp], _ci),
     "attn_swa_sink_prefill_varlen": ([_vp] * 7 + [_ci] * 7 + [_cf, _cf, _ci, _vp], _ci),
     "attn_ga_sink_prefill_varlen": ([_vp] * 7 + [_ci] * 6 + [_cf, _cf, _ci, _vp], _ci),
     "attn_swa_ring_append": ([_vp] * 6 + [_ci] * 6 + [_vp], _ci),
@@ -199,6 +201,30 @@ def attn_ga_sink_prefill_varlen(q, k, v, cu_seqlens, sink, max_seqlen: int | Non
     """Global (full causal) sink attention over a packed batch of sequences."""
     return _prefill_varlen(False, q, k, v, cu_seqlens, sink, 0, max_seqlen, scale, value_scale,
                            out, lse, stream)
+
+
+def attn_sink_prefill_backward(q, k, v, o, lse, dout, sink, window: int = 0,
+                               scale: float | None = None, workspace=None, stream=None):
+    """Gradients of the bf16 prefill: returns (dq, dk, dv, dsink).  o and lse
+    [B,Hq,T] come from the forward call (window 0 = global attention)."""
+    _cuda(q, k, v, o, lse, dout, sink, workspace)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if o.shape != q.shape or dout.shape != q.shape or lse.shape != (B, Hq, T):
+        raise ValueError("o/dout [B,T,Hq,D] and lse [B,Hq,T] must match q")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dsink = torch.empty(Hq, dtype=torch.float32, device=q.device)
+    need = _lib.attn_sink_prefill_backward_workspace(B, T, Hq, D)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check(_lib.attn_sink_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                           _ptr(dout), _ptr(sink), _ptr(dq), _ptr(dk), _ptr(dv),
+                                           _ptr(dsink), _ptr(workspace), ws_bytes, B, T, Hq, Hkv,
+                                           D, int(window), scale, _dtype_code(q),
+                                           _stream(stream)))
+    return dq, dk, dv, dsink
 
 
 def _append_common(k_new, v_new, cu_q, seq_lens, kc, vc):

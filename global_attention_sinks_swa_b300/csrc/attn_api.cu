@@ -234,6 +234,40 @@ ATTN_EXPORT attn_status_t attn_ga_sink_prefill(const void *q, const void *k, con
                           D, 0, scale, 1.f, dtype, stream, false);
 }
 
+ATTN_EXPORT size_t attn_sink_prefill_backward_workspace(int B, int T, int Hq, int D) {
+    if (B <= 0 || T <= 0 || Hq <= 0 || D != 128) return 0;
+    return attn::prefill_backward_workspace(B, T, Hq);
+}
+
+ATTN_EXPORT attn_status_t attn_sink_prefill_backward(
+    const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+    const float *sink, void *dq, void *dk, void *dv, float *dsink, void *workspace,
+    size_t workspace_bytes, int B, int T, int Hq, int Hkv, int D, int window, float scale,
+    attn_dtype_t dtype, void *stream) {
+    if (!q || !k || !v || !o || !lse || !dout || !sink || !dq || !dk || !dv || !dsink)
+        return fail(ATTN_ERR_INVALID_ARG, "null pointer argument");
+    if (B < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0 || window < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "bad sizes B=%d T=%d Hq=%d Hkv=%d D=%d window=%d", B, T,
+                    Hq, Hkv, D, window);
+    if (!(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "scale must be > 0");
+    if (dtype != ATTN_BF16 || D != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "the backward pass supports bf16 with D = 128");
+    if (static_cast<long long>(B) * T * Hq >= (1ll << 31))
+        return fail(ATTN_ERR_UNSUPPORTED, "B*T*Hq must be < 2^31");
+    const void *ptrs[8] = {q, k, v, o, dout, dq, dk, dv};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(ATTN_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+    const size_t need = attn_sink_prefill_backward_workspace(B, T, Hq, D);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(ATTN_ERR_INVALID_ARG, "workspace too small: need %zu bytes", need);
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaError_t e = attn::launch_prefill_backward(q, k, v, o, lse, dout, sink, dq, dk, dv, dsink,
+                                                  workspace, B, T, Hq, Hkv, window, scale,
+                                                  as_stream(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "backward launch");
+}
+
 ATTN_EXPORT attn_status_t attn_swa_sink_prefill_varlen(
     const void *q, const void *k, const void *v, const int32_t *cu_seqlens, const float *sink,
     void *o, float *lse, int B, int total_tokens, int max_seqlen, int Hq, int Hkv, int D,

@@ -46,6 +46,15 @@ int prefill_swa_tc_supported(int G, int window);
 // CTAs of the streaming kernel for a batch of at most max_tiles tiles.
 int prefill_swa_grid(long max_tiles);
 
+// Backward of the bf16 prefill (D = 128, batches of equal length): dq, dk, dv
+// (bf16) and dsink (fp32), from q, k, v, the forward's o and lse, and dout.
+size_t prefill_backward_workspace(int B, int T, int Hq);
+cudaError_t launch_prefill_backward(const void *q, const void *k, const void *v, const void *o,
+                                    const float *lse, const void *dout, const float *sink,
+                                    void *dq, void *dk, void *dv, float *dsink, void *workspace,
+                                    int B, int T, int Hq, int Hkv, int window, float scale,
+                                    cudaStream_t s);
+
 // KV-cache appends (plain 16-byte copies).
 cudaError_t launch_ring_append(const void *k_new, const void *v_new, const int32_t *cu_q,
                                const int32_t *seq_lens, void *ring_k, void *ring_v, int B, int Hkv,

@@ -143,6 +143,27 @@ attn_status_t attn_ga_sink_prefill_varlen(const void *q, const void *k, const vo
                                           int Hq, int Hkv, int D, float scale, float value_scale,
                                           attn_dtype_t dtype, void *stream);
 
+/* ---------------------------------------------------------------- backward ---
+ * Gradients of the bf16 prefill [SINK][ARCH] (the sinks are learnable, so
+ * dsink is part of it), batches of equal length, D = 128:
+ *   inputs  q [B,T,Hq,D], k, v [B,T,Hkv,D], o [B,T,Hq,D] and lse [B,Hq,T] of
+ *           the forward call with the same arguments (lse from its `lse`
+ *           output), dout [B,T,Hq,D] = dL/do, sink [Hq];
+ *   outputs dq [B,T,Hq,D], dk, dv [B,T,Hkv,D] (bf16), dsink [Hq] fp32
+ *           (overwritten, not accumulated);
+ *   window 0 = global attention, else the sliding window; scale as forward.
+ * dS_ij = P_ij (<dout_i, v_j> - D_i) with D_i = <dout_i, o_i> and P from the
+ * lse; dsink_h = -sum_i p_sink,i D_i.  `workspace` (device, 256-byte
+ * aligned, attn_sink_prefill_backward_workspace bytes) holds fp32 dq
+ * partials and D. */
+size_t attn_sink_prefill_backward_workspace(int B, int T, int Hq, int D);
+attn_status_t attn_sink_prefill_backward(const void *q, const void *k, const void *v,
+                                         const void *o, const float *lse, const void *dout,
+                                         const float *sink, void *dq, void *dk, void *dv,
+                                         float *dsink, void *workspace, size_t workspace_bytes,
+                                         int B, int T, int Hq, int Hkv, int D, int window,
+                                         float scale, attn_dtype_t dtype, void *stream);
+
 /* ------------------------------------------------------------ KV caches ---
  * SWA ring [KV][MTP]: ring_k, ring_v [B,Hkv,R,D] with R = ring_slots >=
  * window + q_max - 1 (131 for W = 128, q_max = 4); position p of request b
