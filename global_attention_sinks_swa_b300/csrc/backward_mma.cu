@@ -39,13 +39,13 @@ constexpr int kDsStride = kBQ * 2 + 16;  // bytes per key row of the dS^T tile (
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct __align__(128) BwdSmem {
-    uint8_t k[2][kBK * 128];   // [D half][key][64] bf16, 128-byte rows, swizzled
+    uint8_t k[2][kBK * 128];      // [D half][key][64] bf16, 128-byte rows, swizzled
     uint8_t v[2][kBK * 128];
-    uint8_t q[2][kBQ * 128];   // [D half][row][64]
-    uint8_t dout[2][kBQ * 128];
+    uint8_t q[2][2][kBQ * 128];   // [buffer][D half][row][64]: the next step loads
+    uint8_t dout[2][2][kBQ * 128];  // while this one computes
     uint8_t ds[kBK * kDsStride];  // dS^T [key][row] bf16
-    float lse2[kBQ];              // lse * log2(e) of the step's rows (+inf past T)
-    float delta[kBQ];
+    float lse[2][kBQ];            // the step's rows' lse and D (zero past T)
+    float delta[2][kBQ];
 };
 
 // Byte offset of element (row, d) in a swizzled [rows][64] half tile; d % 8 == 0.
@@ -65,6 +65,29 @@ __device__ __forceinline__ void load_tile(uint8_t *half0, uint8_t *half1,
         if (r < nvalid)
             val = *reinterpret_cast<const uint4 *>(src + ((row0 + r) * H + h) * kD + c * 8);
         *reinterpret_cast<uint4 *>((c < 8 ? half0 : half1) + sw(r, (c & 7) * 8)) = val;
+    }
+}
+
+// Asynchronous form of load_tile for the query-side tiles, with the rows'
+// lse and D; rows at or past T are filled with zeros.
+__device__ __forceinline__ void prefetch_step(BwdSmem &sm, int buf, const __nv_bfloat16 *q,
+                                              const __nv_bfloat16 *dout, const float *lse,
+                                              const float *delta, int b, int h, int i0, int T,
+                                              int Hq) {
+    for (int x = threadIdx.x; x < kBQ * 16; x += kThreads) {
+        const int r = x >> 4, c = x & 15;
+        const bool ok = i0 + r < T;
+        const long off = ((static_cast<long>(b) * T + (ok ? i0 + r : 0)) * Hq + h) * kD + c * 8;
+        const uint32_t o = sw(r, (c & 7) * 8);
+        ptx::cp_async16(sm.q[buf][c >> 3] + o, q + off, ok ? 16u : 0u);
+        ptx::cp_async16(sm.dout[buf][c >> 3] + o, dout + off, ok ? 16u : 0u);
+    }
+    if (threadIdx.x < kBQ) {
+        const int i = i0 + threadIdx.x;
+        const bool ok = i < T;
+        const long li = (static_cast<long>(b) * Hq + h) * T + (ok ? i : 0);
+        ptx::cp_async4(&sm.lse[buf][threadIdx.x], lse + li, ok ? 4u : 0u);
+        ptx::cp_async4(&sm.delta[buf][threadIdx.x], delta + li, ok ? 4u : 0u);
     }
 }
 
@@ -140,20 +163,25 @@ __global__ void __launch_bounds__(kThreads)
         for (int e = 0; e < 4; ++e) dka[n][e] = dva[n][e] = 0.f;
 
     const int kw = warp * 16;  // this warp's first key within the tile
-    for (int hh = 0; hh < G; ++hh) {
-        const int h = g * G + hh;
-        for (int i0 = j0; i0 <= last; i0 += kBQ) {
-            __syncthreads();  // the previous step is done with q, dout, ds
-            const int nq = min(kBQ, T - i0);
-            load_tile<kBQ>(sm.q[0], sm.q[1], q, static_cast<long>(b) * T + i0, nq, Hq, h);
-            load_tile<kBQ>(sm.dout[0], sm.dout[1], dout, static_cast<long>(b) * T + i0, nq, Hq, h);
-            if (threadIdx.x < kBQ) {
-                const int i = i0 + threadIdx.x;
-                const long li = (static_cast<long>(b) * Hq + h) * T + i;
-                sm.lse2[threadIdx.x] = i < T ? lse[li] * kLog2e : INFINITY;
-                sm.delta[threadIdx.x] = i < T ? delta[li] : 0.f;
-            }
-            __syncthreads();
+    // steps: every query head of the group x every 32-row tile in [j0, last]
+    const int nt = (last - j0) / kBQ + 1;
+    const int nsteps = G * nt;
+    prefetch_step(sm, 0, q, dout, lse, delta, b, g * G, j0, T, Hq);
+    ptx::cp_async_commit();
+    for (int step = 0; step < nsteps; ++step) {
+        const int h = g * G + step / nt;
+        const int i0 = j0 + (step % nt) * kBQ;
+        const int buf = step & 1;
+        if (step + 1 < nsteps) {  // the other buffer was released at the end of the last step
+            prefetch_step(sm, buf ^ 1, q, dout, lse, delta, b, g * G + (step + 1) / nt,
+                          j0 + ((step + 1) % nt) * kBQ, T, Hq);
+            ptx::cp_async_commit();
+            ptx::cp_async_wait<1>();
+        } else {
+            ptx::cp_async_wait<0>();
+        }
+        __syncthreads();  // this step's tiles (every thread's copies) have landed
+        {
 
             // ---- S^T = K_w Q^T and dP^T = V_w dO^T: [16 keys x 32 rows]
             float st[4][4], dpt[4][4];
@@ -173,8 +201,8 @@ __global__ void __launch_bounds__(kThreads)
                     const int rB = np * 16 + (lane & 7) + 8 * (lane >> 4);
                     const int dB = kk * 16 + 8 * (mi & 1);
                     uint32_t qb[4], ob[4];
-                    ptx::ldsm_x4(ptx::smem_u32(sm.q[dB >> 6]) + sw(rB, dB & 63), qb[0], qb[1], qb[2], qb[3]);
-                    ptx::ldsm_x4(ptx::smem_u32(sm.dout[dB >> 6]) + sw(rB, dB & 63), ob[0], ob[1], ob[2], ob[3]);
+                    ptx::ldsm_x4(ptx::smem_u32(sm.q[buf][dB >> 6]) + sw(rB, dB & 63), qb[0], qb[1], qb[2], qb[3]);
+                    ptx::ldsm_x4(ptx::smem_u32(sm.dout[buf][dB >> 6]) + sw(rB, dB & 63), ob[0], ob[1], ob[2], ob[3]);
                     ptx::mma_bf16_16816(st[2 * np], ka, qb[0], qb[1]);
                     ptx::mma_bf16_16816(st[2 * np + 1], ka, qb[2], qb[3]);
                     ptx::mma_bf16_16816(dpt[2 * np], va, ob[0], ob[1]);
@@ -188,10 +216,11 @@ __global__ void __launch_bounds__(kThreads)
                 for (int e = 0; e < 4; ++e) {
                     const int r = 8 * n + 2 * cq + (e & 1);
                     const int key = j0 + kw + gq + 8 * (e >> 1);
-                    const bool vis = key_visible(i0 + r, key, window) & (key < T);
-                    const float p = vis ? ptx::exp2_approx(st[n][e] * sl2 - sm.lse2[r]) : 0.f;
+                    const bool vis = key_visible(i0 + r, key, window) & (key < T) & (i0 + r < T);
+                    const float p =
+                        vis ? ptx::exp2_approx(st[n][e] * sl2 - sm.lse[buf][r] * kLog2e) : 0.f;
                     st[n][e] = p;
-                    dpt[n][e] = p * (dpt[n][e] - sm.delta[r]);
+                    dpt[n][e] = p * (dpt[n][e] - sm.delta[buf][r]);
                 }
             // ---- dV += P^T dO, dK += dS^T Q  ([16 keys x 128 d], k = 32 rows)
 #pragma unroll
@@ -210,8 +239,8 @@ __global__ void __launch_bounds__(kThreads)
                 for (int nd = 0; nd < 8; ++nd) {
                     const int dB = nd * 16 + 8 * (lane >> 4);         // n = d
                     uint32_t ob[4], qb[4];
-                    ptx::ldsm_x4_t(ptx::smem_u32(sm.dout[dB >> 6]) + sw(rB, dB & 63), ob[0], ob[1], ob[2], ob[3]);
-                    ptx::ldsm_x4_t(ptx::smem_u32(sm.q[dB >> 6]) + sw(rB, dB & 63), qb[0], qb[1], qb[2], qb[3]);
+                    ptx::ldsm_x4_t(ptx::smem_u32(sm.dout[buf][dB >> 6]) + sw(rB, dB & 63), ob[0], ob[1], ob[2], ob[3]);
+                    ptx::ldsm_x4_t(ptx::smem_u32(sm.q[buf][dB >> 6]) + sw(rB, dB & 63), qb[0], qb[1], qb[2], qb[3]);
                     ptx::mma_bf16_16816(dva[2 * nd], pa, ob[0], ob[1]);
                     ptx::mma_bf16_16816(dva[2 * nd + 1], pa, ob[2], ob[3]);
                     ptx::mma_bf16_16816(dka[2 * nd], sa, qb[0], qb[1]);
@@ -274,6 +303,7 @@ __global__ void __launch_bounds__(kThreads)
                         }
                     }
         }
+        __syncthreads();  // done with this step's buffer and ds before they are refilled
     }
     // ---- dK (x scale) and dV of this warp's 16 keys
 #pragma unroll
