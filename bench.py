@@ -313,15 +313,15 @@ def bench_prefill_packed(A, synth, steps: int, warmup: int, world: int, stream, 
     return ms, flop, nbytes, lens
 
 
-def bench_backward(A, synth, steps: int, warmup: int, world: int, stream, seed: int):
-    """SWA backward (dq, dk, dv, dsink) at the headline sizes; FLOP = the five
-    products over visible pairs (S, dP, dV, dK, dQ): 10*D*Hq per pair."""
+def bench_backward(A, synth, steps: int, warmup: int, world: int, stream, seed: int, T_=T):
+    """SWA backward (dq, dk, dv, dsink), by default at the headline sizes; FLOP
+    = the five products over visible pairs (S, dP, dV, dK, dQ): 10*D*Hq per pair."""
     import torch
-    q, k, v, sink = synth.prefill_inputs(B, T, HQ, HKV, D, seed, device="cuda")
-    dout = synth.normal((B, T, HQ, D), seed + 1, device="cuda")
-    lse = torch.empty(B, HQ, T, device="cuda")
+    q, k, v, sink = synth.prefill_inputs(B, T_, HQ, HKV, D, seed, device="cuda")
+    dout = synth.normal((B, T_, HQ, D), seed + 1, device="cuda")
+    lse = torch.empty(B, HQ, T_, device="cuda")
     o = A.attn_swa_sink_prefill(q, k, v, sink, window=W, lse=lse, stream=stream)
-    ws = torch.empty(A._lib.attn_sink_prefill_backward_workspace(B, T, HQ, D), dtype=torch.uint8,
+    ws = torch.empty(A._lib.attn_sink_prefill_backward_workspace(B, T_, HQ, D), dtype=torch.uint8,
                      device="cuda")
 
     def step(_):
@@ -334,7 +334,7 @@ def bench_backward(A, synth, steps: int, warmup: int, world: int, stream, seed: 
         ms = time_region(step, steps, world, stream)
     if A.attn_check_device_error(stream) != 0:
         raise RuntimeError("backward reported a device error")
-    return ms, 10.0 * D * HQ * visible_pairs(T, W) * B
+    return ms, 10.0 * D * HQ * visible_pairs(T_, W) * B
 
 
 def bench_prefill_e2e(A, synth, steps: int, warmup: int, world: int, stream, seed: int):
@@ -519,7 +519,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-parts", action="store_true", help="headline only")
     ap.add_argument("--profile", default="",
-                    help="comma list of swa,ga,verify_ga,verify_swa: run only these kernels "
+                    help="comma list of swa,ga,verify_ga,verify_ga_fp8,verify_swa,backward: run only these kernels "
                          "(warmup + steps), no JSON line; for ncu captures")
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -661,6 +661,8 @@ def run_profile(A, synth, args, warmup, stream):
     for name in args.profile.split(","):
         if name in ("swa", "ga"):
             bench_prefill(A, synth, name, args.steps, warmup, 1, stream, 1002)
+        elif name == "backward":   # a quarter of the headline length: a small capture
+            bench_backward(A, synth, args.steps, warmup, 1, stream, 1008, T_=T // 4)
         elif name in ("verify_ga", "verify_ga_fp8"):
             ctx = synth.context_lengths(16, 4096, 65536, 1004)
             bench_verify_ga(A, ctx, np.full(16, QMAX, np.int32), args.steps, warmup, 1, stream, 1004,
