@@ -153,3 +153,19 @@ def test_host_rejects_bad_arguments():
     with pytest.raises(A.AttnError) as e:
         A.attn_ga_sink_prefill_varlen(q, k, k, cu, sink, max_seqlen=10, value_scale=math.inf)
     assert e.value.status == A.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kind", ["swa", "ga"])
+def test_many_sequences(kind):
+    """100 sequences (zeros among them): the streaming kernel locates each CTA's
+    first tile with a warp scan over chunks of 32 sequences."""
+    lens = synth.packed_lengths(100, 1, 300, 1234)
+    lens[::7] = 0
+    lens[3] = 17
+    q, k, v, sink, cu = synth.packed_inputs(lens, 64 if kind == "swa" else 16,
+                                            8 if kind == "swa" else 2, 128, seed=1235)
+    o, lse = _run(kind, q.cuda(), k.cuda(), v.cuda(), cu, sink.cuda(), 128 if kind == "swa" else 0)
+    ref, ref_lse = oracle.prefill_varlen(q, k, v, cu, sink, 128 if kind == "swa" else None,
+                                         want_lse=True)
+    assert_bf16_close(o, ref, f"{kind} 100 sequences")
+    assert_bf16_close(lse, ref_lse, f"{kind} 100 sequences lse")

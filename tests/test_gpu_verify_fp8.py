@@ -146,3 +146,25 @@ def test_full_size_fp8_verify_sampled():
         r = oracle.verify_fp8(q[r0:r1].cpu(), np.array([0, r1 - r0], np.int32), kh, vh, ks.cpu(),
                               vs.cpu(), np.array([L], np.int32), sink.cpu(), None)
         assert_bf16_close(o[r0:r1], r, f"fp8 full size request {b}")
+
+
+def test_fp8_bad_page_ids_are_reported():
+    """A page id outside the pool sets ATTN_DEVERR_PAGE_OOB in the 8-bit append
+    and verify, and the context stays usable."""
+    A.attn_check_device_error()
+    num_pages = 4
+    pt = torch.tensor([[0, 1], [2, 77]], dtype=torch.int32, device="cuda")
+    seq_lens = torch.tensor([100, 100], dtype=torch.int32, device="cuda")
+    cu_q = torch.tensor([0, 4, 8], dtype=torch.int32, device="cuda")
+    kp = torch.zeros(num_pages, Hkv, PAGE, D, dtype=torch.uint8, device="cuda")
+    vp = kp.clone()
+    ks = torch.full((Hkv,), 0.02, device="cuda")
+    new = synth.normal((8, Hkv, D), 1, device="cuda")
+    A.attn_ga_paged_append_fp8(new, new.clone(), cu_q, seq_lens, kp, vp, pt, ks, ks, q_max=QMAX)
+    assert A.attn_check_device_error() & A.DEVERR_PAGE_OOB
+    q = synth.normal((8, Hq, D), 2, device="cuda")
+    sink = synth.sink_logits(Hq, 3, device="cuda")
+    A.attn_ga_sink_verify_fp8(q, cu_q, kp, vp, pt, seq_lens, sink, ks, ks, max_ctx=128, q_max=QMAX)
+    assert A.attn_check_device_error() & A.DEVERR_PAGE_OOB
+    assert A.attn_check_device_error() == 0
+    assert torch.isfinite(torch.ones(4, device="cuda").sum())
