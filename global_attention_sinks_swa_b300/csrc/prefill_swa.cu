@@ -23,11 +23,14 @@
 // Roles (352 threads):
 //   warps 0-3 / 4-7  softmax + epilogue of the tiles in TMEM slot 0 / slot 1
 //                    (thread = row = TMEM lane);
-//   warp 8           TMA producer of Q (4-stage ring) and K blocks;
+//   warp 8           TMA producer of Q (3-stage ring) and K blocks (a K block
+//                    in ring slot 0..7 is loaded twice: slot and mirror);
 //   warp 10          TMA producer of V blocks;
 //   warp 9           one thread issues tcgen05.mma: S = Q K^T (bf16 operands
-//                    in 128-byte-swizzled shared memory, fp32 S in TMEM; split
-//                    in two MMAs where the window wraps around the ring) and
+//                    in 128-byte-swizzled shared memory, fp32 S in TMEM; the
+//                    K blocks of ring slots 0..7 are also kept at slots
+//                    12..19, so a tile's nine blocks are always contiguous
+//                    and S is one N = 144 MMA per k-step) and
 //                    O = P V (P as bf16 in TMEM over the S columns), choosing
 //                    whichever of the next S and the next PV is ready.
 // Per TMEM slot (256 columns): S in columns 0..143, P (bf16 pairs) in 0..71,
@@ -53,19 +56,21 @@ constexpr int kTT = kSwaTokens;                // tokens per tile
 constexpr int kN = kSwaKeys;                   // keys per tile
 constexpr int kNB = kSwaTileBlocks;            // key blocks per tile
 constexpr int kRing = kSwaRingBlocks;          // K/V ring blocks
-constexpr int kQStages = 4;
+constexpr int kQStages = 3;
 constexpr int kQHalf = 128 * kHalfRowBytes;    // 16 KB: 128 rows of one D half
 constexpr int kBlkHalf = kSwaBlockKeys * kHalfRowBytes;  // 2 KB: one block, one D half
 constexpr int kRingHalf = kRing * kBlkHalf;    // one D half of the ring
+constexpr int kKRingHalf = (kRing + kNB - 1) * kBlkHalf;  // K ring with its mirror
 constexpr int kThreads = 352;
 constexpr int kOCol = 96;                      // O accumulator column in a slot
+constexpr uint32_t kIdescS = ptx::idesc_bf16(128, kN, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, 128, false, true);
 static_assert(kOCol >= kN / 2 && kOCol + 128 <= 256, "slot TMEM layout");
 static_assert(kRing >= kNB + 1, "ring must hold a tile's window plus one block");
 
 struct __align__(1024) Smem {
     uint8_t q[kQStages][2][kQHalf];   // [stage][D half]
-    uint8_t k[2][kRingHalf];          // [D half][ring block][16 rows]
+    uint8_t k[2][kKRingHalf];         // [D half][ring block (+ mirror of 0..7)][16 rows]
     uint8_t v[2][kRingHalf];
     uint64_t q_full[kQStages], q_empty[kQStages];
     uint64_t k_full[kRing], k_empty[kRing], v_full[kRing], v_empty[kRing];
@@ -265,11 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&full[slot], 2 * kBlkHalf);
+                    const bool mirror = qk && slot < kNB - 1;
+                    const int half = qk ? kKRingHalf : kRingHalf;
+                    ptx::mbar_arrive_expect_tx(&full[slot], (mirror ? 4 : 2) * kBlkHalf);
                     const int kp = key0 + kSwaBlockKeys * (s - cur.base);
-                    for (int hf = 0; hf < 2; ++hf)
-                        ptx::tma_load_3d(ring + hf * kRingHalf + slot * kBlkHalf, map, hf * 64, t.g,
+                    for (int hf = 0; hf < 2; ++hf) {
+                        ptx::tma_load_3d(ring + hf * half + slot * kBlkHalf, map, hf * 64, t.g,
                                          t.start + kp, &full[slot]);
+                        if (mirror)
+                            ptx::tma_load_3d(ring + hf * half + (slot + kRing) * kBlkHalf, map,
+                                             hf * 64, t.g, t.start + kp, &full[slot]);
+                    }
                     last_s = s;
                 }
             }
@@ -331,19 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                          ptx::mbar_test(ptx::smem_u32(&sm.tmem_free[s]), ((is.k >> 1) - 1) & 1))) {
                         ptx::tc_fence_after();
                         const uint32_t tS = tmem + 256 * s;
-                        const int r = is.cur.base % kRing;
-                        const int n1 = (kRing - r < kNB) ? kRing - r : kNB;  // blocks before the wrap
-                        const uint32_t id1 = ptx::idesc_bf16(128, n1 * kSwaBlockKeys, false, false);
-                        const uint32_t id2 =
-                            ptx::idesc_bf16(128, (kNB - n1) * kSwaBlockKeys, false, false);
+                        const int r = is.cur.base % kRing;  // blocks r..r+8: contiguous (mirror)
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint64_t ad = kmajor_desc(sm.q[st][kk >> 2], kk & 3);
                             const uint32_t kb = kbase[kk >> 2] + (kk & 3) * 32;
-                            ptx::mma_ss(tS, ad, ptx::sdesc_sw128(kb + r * kBlkHalf, 16, 1024), id1,
+                            ptx::mma_ss(tS, ad, ptx::sdesc_sw128(kb + r * kBlkHalf, 16, 1024), kIdescS,
                                         kk > 0 ? 1u : 0u);
-                            if (n1 < kNB)
-                                ptx::mma_ss(tS + n1 * kSwaBlockKeys, ad, ptx::sdesc_sw128(kb, 16, 1024),
-                                            id2, kk > 0 ? 1u : 0u);
                         }
                         ptx::tc_commit(&sm.s_full[s]);
                         ptx::tc_commit(&sm.q_empty[st]);
