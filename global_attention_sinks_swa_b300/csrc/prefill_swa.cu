@@ -386,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + 256 * s + lane_off, tO = tS + kOCol;
         const int t_in = row / kG, hh = row % kG;
         const float sl2 = scale * kLog2e;
+        const bool out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;  // 32-byte stores
         SwaTileCursor t = first;
         if (s == 1 && n > 1) swa_cursor_next(t, cu, B, T, total, Hkv);
         for (int k = s; k < n; k += 2) {
@@ -464,15 +465,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint4 *dst = reinterpret_cast<uint4 *>(
                     out + (static_cast<long>(t.start + qpos) * Hq + h) * 128);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    uint32_t w[4];
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t w[8];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int c = 8 * i + 2 * j;
+                    for (int j = 0; j < 8; ++j) {
+                        const int c = 16 * i + 2 * j;
                         const float2 y = f2_split(f2_mul(f2(o[c], o[c + 1]), inv2));
                         w[j] = ptx::pack_bf16x2(y.x, y.y);
                     }
-                    dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                    if (out32) {  // one 32-byte store: a whole sector of the row
+                        ptx::st_global_v8(dst + 2 * i, w);
+                    } else {
+                        dst[2 * i] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[2 * i + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
                 }
                 if (lse)
                     lse[lse_index(cu, t.b, h, qpos, t.start, T, total, Hq)] =
