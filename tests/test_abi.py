@@ -49,3 +49,27 @@ def test_verify_workspace_size_formula():
     n = A.attn_ga_sink_verify_workspace(64, 64, 8, 128, 4, 65536)
     units = 64 * 8 * 16
     assert n >= units * 32 * 130 * 4
+
+
+def test_new_entry_points_reject_null_pointers_on_host():
+    L = A._lib
+    f32 = ctypes.c_float
+    # packed prefill: 7 pointers, then B, total, max_seqlen, Hq, Hkv, D, (window), scale, vscale
+    assert L.attn_swa_sink_prefill_varlen(*([None] * 7), 1, 16, 16, 8, 1, 128, 128, f32(0.1),
+                                          f32(1.0), 0, None) == A.ATTN_ERR_INVALID_ARG
+    assert L.attn_ga_sink_prefill_varlen(*([None] * 7), 1, 16, 16, 8, 1, 128, f32(0.1), f32(1.0),
+                                         0, None) == A.ATTN_ERR_INVALID_ARG
+    # backward: 12 pointers, workspace bytes, B, T, Hq, Hkv, D, window, scale, dtype, stream
+    assert L.attn_sink_prefill_backward(*([None] * 12), 0, 1, 16, 8, 1, 128, 128, f32(0.1), 0,
+                                        None) == A.ATTN_ERR_INVALID_ARG
+    # 8-bit append and verify
+    assert L.attn_ga_paged_append_fp8(*([None] * 7), 4, 4, 64, None, None, 1, 8, 128, 4,
+                                      None) == A.ATTN_ERR_INVALID_ARG
+    assert L.attn_ga_sink_verify_fp8(*([None] * 5), 4, 4, 64, *([None] * 6), 0, 1, 64, 8, 128, 4,
+                                     4096, f32(0.1), None) == A.ATTN_ERR_INVALID_ARG
+    assert b"null" in L.attn_last_error()
+
+
+def test_backward_workspace_size():
+    assert A._lib.attn_sink_prefill_backward_workspace(1, 1024, 64, 128) >= 1024 * 64 * 128 * 4 + 64 * 1024 * 4
+    assert A._lib.attn_sink_prefill_backward_workspace(1, 1024, 64, 64) == 0   # unsupported D
