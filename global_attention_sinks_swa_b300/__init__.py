@@ -61,6 +61,7 @@ _SIGS = {
     "attn_debug_prefill_visits": ([_vp] + [_ci] * 4 + [_vp], _ci),
     "attn_debug_swa_stream_visits": ([_vp] + [_ci] * 5 + [_vp], _ci),
     "attn_debug_verify_positions": ([_vp, _ci, _vp, _vp] + [_ci] * 6 + [_vp], _ci),
+    "attn_debug_wait_timeout": ([_vp], _ci),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -406,3 +407,9 @@ def attn_debug_verify_positions(kind: int, cu_q, seq_lens, q_max: int, window: i
                                             int(q_max), int(window), int(ring_slots),
                                             int(max_pages), int(page_size), _stream(stream)))
     return out
+
+
+def attn_debug_wait_timeout(stream=None):
+    """Enqueue a kernel whose pipeline wait runs out (about 2 s) and sets
+    DEVERR_WAIT_TIMEOUT; read and clear it with attn_check_device_error()."""
+    _check(_lib.attn_debug_wait_timeout(_stream(stream)))

@@ -571,3 +571,14 @@ ATTN_EXPORT attn_status_t attn_debug_verify_positions(int32_t *out, int kind, co
                                                         as_stream(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "debug verify positions");
 }
+
+namespace attn {
+cudaError_t launch_debug_wait_timeout(unsigned *err, cudaStream_t s);  // debug_index.cu
+}
+
+ATTN_EXPORT attn_status_t attn_debug_wait_timeout(void *stream) {
+    unsigned *err = device_error_word();
+    if (!err) return fail(ATTN_ERR_CUDA, "no CUDA device / error word unavailable");
+    cudaError_t e = attn::launch_debug_wait_timeout(err, as_stream(stream));
+    return e == cudaSuccess ? ok() : cuda_fail(e, "debug wait timeout");
+}

@@ -4,6 +4,7 @@
 // j >= i - W + 1; ring slot p mod R; page page_table[b][p / P]).
 #include "index_math.cuh"
 #include "internal.h"
+#include "tc_tile.cuh"
 
 namespace attn {
 namespace {
@@ -118,6 +119,19 @@ __global__ void verify_positions_kernel(int32_t *out, int kind, const int32_t *c
     }
 }
 
+// A pipeline wait that nothing completes: thread 0 waits on a fresh mbarrier
+// with the kernels' bounded wait, which gives up after its time limit and
+// records the wait-timeout bit exactly as a stalled pipeline would.
+__global__ void wait_timeout_kernel(unsigned *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0)) atomicOr(err, tc::kErrWait);
+}
+
 }  // namespace
 
 cudaError_t launch_debug_prefill_visits(int32_t *visits, int mode, int T, int window, int G,
@@ -149,6 +163,11 @@ cudaError_t launch_debug_verify_positions(int32_t *out, int kind, const int32_t 
     if (B == 0 || q_max == 0) return cudaSuccess;
     verify_positions_kernel<<<dim3(B, q_max), 128, 0, s>>>(out, kind, cu_q, seq_lens, q_max,
                                                           window, R, max_pages, page_size);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_wait_timeout(unsigned *err, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 32, 0, s>>>(err);
     return cudaGetLastError();
 }
 

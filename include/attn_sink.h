@@ -307,6 +307,15 @@ attn_status_t attn_debug_verify_positions(int32_t *out, int kind, const int32_t 
                                           int ring_slots, int max_pages, int page_size,
                                           void *stream);
 
+/* attn_debug_wait_timeout: enqueues one kernel whose only pipeline wait (an
+ * mbarrier phase that nothing completes) runs out after the kernels' wait
+ * limit of 2 s and sets ATTN_DEVERR_WAIT_TIMEOUT in the device error word, as
+ * a stalled pipeline would.  Kernels launched while that bit is set return
+ * without doing any work; attn_check_device_error() reports and clears it.
+ * For tests of the failure path: no trap, no fault, and the context stays
+ * usable.  Errors: ATTN_ERR_CUDA if no device is current or the launch fails. */
+attn_status_t attn_debug_wait_timeout(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

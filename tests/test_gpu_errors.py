@@ -1,10 +1,12 @@
 """Failure reporting without a GPU fault: bad inputs that only the device can
 see set bits in the device error word (the offending work is skipped, no trap,
-no hang), and host-detectable errors return a status before any launch."""
+no hang), a pipeline wait that nothing completes gives up after its time limit,
+and host-detectable errors return a status before any launch."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 
 A = pytest.importorskip("global_attention_sinks_swa_b300")
@@ -48,6 +50,24 @@ def test_qlen_above_qmax_and_short_context_set_bits():
     A.attn_swa_sink_verify(q, cu_q, ring, ring.clone(), seq_lens, sink, window=128, q_max=4)
     bits = A.attn_check_device_error()
     assert bits & A.DEVERR_QLEN and bits & A.DEVERR_CTX_OOB
+
+
+def test_wait_timeout_sets_bit_then_launches_skip_until_cleared():
+    _clear()
+    q, k, v, sink = synth.prefill_inputs(1, 256, Hq, Hkv, D, 17)
+    q, k, v, sink = q.cuda(), k.cuda(), v.cuda(), sink.cuda()
+    # a wait that nothing completes runs out (about 2 s) and sets the bit
+    A.attn_debug_wait_timeout()
+    o = torch.full_like(q, float("nan"))
+    A.attn_swa_sink_prefill(q, k, v, sink, window=128, out=o)
+    assert A.attn_check_device_error() & A.DEVERR_WAIT_TIMEOUT
+    assert torch.isnan(o.float()).all()  # launched while the bit was set: no work done
+    # reading the word cleared it; the same call now computes
+    assert A.attn_check_device_error() == 0
+    A.attn_swa_sink_prefill(q, k, v, sink, window=128, out=o)
+    assert A.attn_check_device_error() == 0
+    ref = oracle.prefill(q.cpu(), k.cpu(), v.cpu(), sink.cpu(), 128)
+    assert np.abs(o.float().cpu().numpy() - ref).max() < 2e-2
 
 
 def test_host_side_errors_return_status():
