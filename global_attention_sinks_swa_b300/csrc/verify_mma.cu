@@ -128,11 +128,6 @@ __device__ __forceinline__ int acc_d(int i, int c) {
     else return 8 * i + 2 * c;
 }
 
-// Two E4M3 codes (bytes lo, hi of x) -> f16x2 B operand.
-__device__ __forceinline__ uint32_t codes_f16x2(uint32_t x, uint32_t sel) {
-    return ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(x, 0u, sel) & 0xffffu));
-}
-
 template <bool FP8>
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -428,10 +423,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {  // d-chunk 2dp + h: registers 2h, 2h+1
                             const int nd = 2 * dp + h;
-                            mma16816<true>(oacc[2 * nd], pa, codes_f16x2(r[2 * h], 0x20u),
-                                           codes_f16x2(r[2 * h + 1], 0x20u));
-                            mma16816<true>(oacc[2 * nd + 1], pa, codes_f16x2(r[2 * h], 0x31u),
-                                           codes_f16x2(r[2 * h + 1], 0x31u));
+                            // bytes (0, 2) -> even d, bytes (1, 3) -> odd d: one permute, two converts
+                            uint32_t e0, o0, e1, o1;
+                            ptx::e4m3x4_to_f16x2x2(__byte_perm(r[2 * h], 0u, 0x3120u), e0, o0);
+                            ptx::e4m3x4_to_f16x2x2(__byte_perm(r[2 * h + 1], 0u, 0x3120u), e1, o1);
+                            mma16816<true>(oacc[2 * nd], pa, e0, e1);
+                            mma16816<true>(oacc[2 * nd + 1], pa, o0, o1);
                         }
                     }
                 } else {
