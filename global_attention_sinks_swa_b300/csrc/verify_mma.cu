@@ -365,18 +365,31 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
-            // mask, scale to log2 units, online softmax
+            // mask, scale to log2 units, online softmax.  A page that ends at or
+            // before the first draft's position is visible to every query row:
+            // only padding rows are masked there
             float mx[2] = {-INFINITY, -INFINITY};
+            if (kind == 1 && (src.pb + blk + 1) * kVerifyBlock - 1 <= L - q_len) {
 #pragma unroll
-            for (int n = 0; n < 4; ++n)
+                for (int n = 0; n < 4; ++n)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = kh * 32 + n * 8 + 2 * (lane & 3) + (e & 1);
-                    const int p = src.position(blk, c);
-                    const float val = key_visible(qpos[e >> 1], p, win) ? s[n][e] * sl2 : -INFINITY;
-                    s[n][e] = val;
-                    mx[e >> 1] = fmaxf(mx[e >> 1], val);
-                }
+                    for (int e = 0; e < 4; ++e) {
+                        const float val = qpos[e >> 1] >= 0 ? s[n][e] * sl2 : -INFINITY;
+                        s[n][e] = val;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], val);
+                    }
+            } else {
+#pragma unroll
+                for (int n = 0; n < 4; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = kh * 32 + n * 8 + 2 * (lane & 3) + (e & 1);
+                        const int p = src.position(blk, c);
+                        const float val = key_visible(qpos[e >> 1], p, win) ? s[n][e] * sl2 : -INFINITY;
+                        s[n][e] = val;
+                        mx[e >> 1] = fmaxf(mx[e >> 1], val);
+                    }
+            }
             float alpha[2], mbase[2];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
