@@ -1,6 +1,7 @@
 """The C-ABI library loads on a CPU host and exports every declared entry
 point; argument errors are reported from the host before any CUDA work."""
 import ctypes
+import os
 import subprocess
 
 import pytest
@@ -73,3 +74,20 @@ def test_new_entry_points_reject_null_pointers_on_host():
 def test_backward_workspace_size():
     assert A._lib.attn_sink_prefill_backward_workspace(1, 1024, 64, 128) >= 1024 * 64 * 128 * 4 + 64 * 1024 * 4
     assert A._lib.attn_sink_prefill_backward_workspace(1, 1024, 64, 64) == 0   # unsupported D
+
+
+def test_package_refuses_to_import_without_its_library(tmp_path):
+    """No CPU fallback: a copy of the binding with no library next to it fails
+    at import with a message naming the build step."""
+    import importlib.util
+    import shutil
+
+    import global_attention_sinks_swa_b300 as A
+    pkg = tmp_path / "pkg_copy"
+    pkg.mkdir()
+    shutil.copy(os.path.join(os.path.dirname(A.__file__), "__init__.py"), pkg / "__init__.py")
+    spec = importlib.util.spec_from_file_location("pkg_copy", pkg / "__init__.py",
+                                                  submodule_search_locations=[str(pkg)])
+    mod = importlib.util.module_from_spec(spec)
+    with pytest.raises(ImportError, match="no CPU fallback"):
+        spec.loader.exec_module(mod)
