@@ -109,6 +109,14 @@ def _cuda(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _expect(t, shape, dtype, what):
+    """The library trusts the sizes it is given: every buffer must match them."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape) or (dtype is not None and t.dtype != dtype):
+        raise ValueError(f"{what} must be {dtype} {list(shape)}, got {t.dtype} {list(t.shape)}")
+
+
 def attn_version() -> int:
     return _lib.attn_version()
 
@@ -130,6 +138,7 @@ def _prefill(swa: bool, q, k, v, sink, window, scale, out, lse, stream):
         raise ValueError("shapes: q [B,T,Hq,D], k/v [B,T,Hkv,D], sink [Hq]")
     if k.dtype != q.dtype or v.dtype != q.dtype or sink.dtype != torch.float32:
         raise TypeError("q/k/v share one dtype; sink is float32")
+    _expect(out, q.shape, q.dtype, "out")
     out = torch.empty_like(q) if out is None else out
     if lse is not None and (lse.shape != (B, Hq, T) or lse.dtype != torch.float32):
         raise ValueError("lse must be float32 [B,Hq,T]")
@@ -170,6 +179,7 @@ def _prefill_varlen(swa: bool, q, k, v, cu_seqlens, sink, window, max_seqlen, sc
         raise TypeError("cu_seqlens is int32")
     if max_seqlen is None:  # one device-to-host read; pass it to stay asynchronous
         max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if B > 0 else 0
+    _expect(out, q.shape, q.dtype, "out")
     out = torch.empty_like(q) if out is None else out
     if lse is not None and (lse.shape != (Hq, total) or lse.dtype != torch.float32):
         raise ValueError("lse must be float32 [Hq,total]")
@@ -213,6 +223,12 @@ def attn_sink_prefill_backward(q, k, v, o, lse, dout, sink, window: int = 0,
     Hkv = k.shape[2]
     if o.shape != q.shape or dout.shape != q.shape or lse.shape != (B, Hq, T):
         raise ValueError("o/dout [B,T,Hq,D] and lse [B,Hq,T] must match q")
+    for t, name in ((k, "k"), (v, "v")):
+        _expect(t, (B, T, Hkv, D), q.dtype, name)
+    for t, name in ((o, "o"), (dout, "dout")):
+        _expect(t, q.shape, q.dtype, name)
+    _expect(lse, (B, Hq, T), torch.float32, "lse")
+    _expect(sink, (Hq,), torch.float32, "sink")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dsink = torch.empty(Hq, dtype=torch.float32, device=q.device)
     need = _lib.attn_sink_prefill_backward_workspace(B, T, Hq, D)
@@ -234,6 +250,9 @@ def _append_common(k_new, v_new, cu_q, seq_lens, kc, vc):
         raise TypeError("cu_q and seq_lens are int32")
     if k_new.dtype != kc.dtype or v_new.dtype != vc.dtype or k_new.shape != v_new.shape:
         raise TypeError("new keys/values must match the cache dtype and each other")
+    if k_new.dim() != 3 or seq_lens.dim() != 1:
+        raise ValueError("k_new/v_new [rows,Hkv,D], seq_lens [B]")
+    _expect(cu_q, (seq_lens.shape[0] + 1,), torch.int32, "cu_q")
     return seq_lens.shape[0], k_new.shape[1], k_new.shape[2]
 
 
@@ -272,6 +291,12 @@ def attn_swa_sink_verify(q, cu_q, ring_k, ring_v, seq_lens, sink, window: int = 
     B, Hkv, R, _ = ring_k.shape
     if cu_q.shape != (B + 1,) or seq_lens.shape != (B,) or sink.shape != (Hq,):
         raise ValueError("cu_q [B+1], seq_lens [B], sink [Hq]")
+    _expect(ring_k, (B, Hkv, R, D), q.dtype, "ring_k")
+    _expect(ring_v, (B, Hkv, R, D), q.dtype, "ring_v")
+    _expect(cu_q, (B + 1,), torch.int32, "cu_q")
+    _expect(seq_lens, (B,), torch.int32, "seq_lens")
+    _expect(sink, (Hq,), torch.float32, "sink")
+    _expect(out, q.shape, q.dtype, "out")
     out = torch.empty_like(q) if out is None else out
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     _check(_lib.attn_swa_sink_verify(_ptr(q), _ptr(cu_q), _ptr(ring_k), _ptr(ring_v),
@@ -286,14 +311,27 @@ def attn_ga_sink_verify_workspace(B: int, Hq: int, Hkv: int, D: int, q_max: int,
     return int(_lib.attn_ga_sink_verify_workspace(B, Hq, Hkv, D, q_max, max_ctx))
 
 
+def _paged_checks(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, out, page_dtype):
+    nq, Hq, D = q.shape
+    P, Hkv, page_size, _ = k_pages.shape
+    B, max_pages = page_table.shape
+    _expect(k_pages, (P, Hkv, page_size, D), page_dtype, "k_pages")
+    _expect(v_pages, (P, Hkv, page_size, D), page_dtype, "v_pages")
+    _expect(page_table, (B, max_pages), torch.int32, "page_table")
+    _expect(cu_q, (B + 1,), torch.int32, "cu_q")
+    _expect(seq_lens, (B,), torch.int32, "seq_lens")
+    _expect(sink, (Hq,), torch.float32, "sink")
+    _expect(out, q.shape, q.dtype, "out")
+    return nq, Hq, D, P, Hkv, page_size, B, max_pages
+
+
 def attn_ga_sink_verify(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, max_ctx: int,
                         q_max: int = 4, scale: float | None = None, out=None, workspace=None,
                         stream=None):
     """MTP verify against the GA paged cache (split-KV + LSE merge)."""
     _cuda(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, out, workspace)
-    nq, Hq, D = q.shape
-    P, Hkv, page_size, _ = k_pages.shape
-    B, max_pages = page_table.shape
+    nq, Hq, D, P, Hkv, page_size, B, max_pages = _paged_checks(
+        q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, out, q.dtype)
     out = torch.empty_like(q) if out is None else out
     need = attn_ga_sink_verify_workspace(B, Hq, Hkv, D, q_max, max_ctx)
     if workspace is None and need:
@@ -318,9 +356,10 @@ def attn_ga_sink_verify_fp8(q, cu_q, k_pages, v_pages, page_table, seq_lens, sin
         raise TypeError("8-bit pages are uint8 E4M3 codes")
     if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
         raise TypeError("k_scale/v_scale are float32 [Hkv]")
-    nq, Hq, D = q.shape
-    P, Hkv, page_size, _ = k_pages.shape
-    B, max_pages = page_table.shape
+    nq, Hq, D, P, Hkv, page_size, B, max_pages = _paged_checks(
+        q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, out, torch.uint8)
+    _expect(k_scale, (Hkv,), torch.float32, "k_scale")
+    _expect(v_scale, (Hkv,), torch.float32, "v_scale")
     out = torch.empty_like(q) if out is None else out
     need = attn_ga_sink_verify_workspace(B, Hq, Hkv, D, q_max, max_ctx)
     if workspace is None and need:
@@ -348,6 +387,13 @@ def attn_ga_paged_append_fp8(k_new, v_new, cu_q, seq_lens, k_pages, v_pages, pag
         raise TypeError("cu_q, seq_lens and page_table are int32")
     B = seq_lens.shape[0]
     Hkv, D = k_new.shape[1], k_new.shape[2]
+    if k_new.dim() != 3 or k_pages.dim() != 4 or k_pages.shape[1] != Hkv or k_pages.shape[3] != D:
+        raise ValueError("k_new/v_new [rows,Hkv,D], k_pages/v_pages [P,Hkv,page,D]")
+    if page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("page_table must be int32 [B,max_pages]")
+    _expect(cu_q, (B + 1,), torch.int32, "cu_q")
+    _expect(k_scale, (Hkv,), torch.float32, "k_scale")
+    _expect(v_scale, (Hkv,), torch.float32, "v_scale")
     _check(_lib.attn_ga_paged_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(cu_q), _ptr(seq_lens),
                                          _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
                                          page_table.shape[1], k_pages.shape[0], k_pages.shape[2],
@@ -362,9 +408,8 @@ def attn_ga_sink_verify_noalloc(q, cu_q, k_pages, v_pages, page_table, seq_lens,
     split-KV scratch is the library's static 64 MiB device array (see the C
     header for its limits; concurrent calls on one device race on it)."""
     _cuda(q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, out)
-    nq, Hq, D = q.shape
-    P, Hkv, page_size, _ = k_pages.shape
-    B, max_pages = page_table.shape
+    nq, Hq, D, P, Hkv, page_size, B, max_pages = _paged_checks(
+        q, cu_q, k_pages, v_pages, page_table, seq_lens, sink, out, q.dtype)
     if out is None:
         raise ValueError("pass a preallocated `out` (this entry point allocates nothing)")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
