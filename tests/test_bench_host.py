@@ -1,0 +1,58 @@
+"""Host-side parts of bench.py that need no GPU: the reference arm's JSON line
+(the oracle timed on the host cores) and the clock sampler's parsing of
+nvidia-smi lines into a median clock and the set of throttle reasons seen."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["n_gpus"] == 1
+    assert line["steps"] == 1 and line["warmup"] >= 3          # at least three warm-up steps
+    assert line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
+    assert line["higher_is_better"] is True and line["dtype"] == "f64"
+    assert "workload" in line["config"] and "model" not in line["config"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+class _FakeProc:
+    def __init__(self, lines):
+        self.stdout = iter(lines)
+
+
+def test_clock_sampler_parses_nvidia_smi_lines():
+    s = bench.ClockSampler(0)
+    s._first = type("E", (), {"set": lambda self: None})()
+    s._proc = _FakeProc([
+        "2032, 2032, Not Active, Not Active, Not Active, Not Active\n",
+        "1965, 2032, Not Active, Not Active, Not Active, Active\n",
+        "garbage line\n",
+        "[N/A], 2032, Not Active, Not Active, Not Active, Not Active\n",
+        "1890, 2032, Active, Not Active, Not Active, Active\n",
+    ])
+    s._smi_read()
+    out = s.summary()
+    assert out["samples"] == 3 and out["sm_max_mhz"] == 2032.0
+    assert out["sm_mhz"] == 1965.0
+    assert out["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_clock_sampler_without_samples_reports_none():
+    out = bench.ClockSampler(0).summary()
+    assert out["sm_mhz"] is None and out["reasons"] == [] and out["samples"] == 0
