@@ -3,8 +3,9 @@ formulation: full score matrix, -inf outside the mask, an appended sink column,
 scipy softmax) over many small random configurations: batch, length (ragged,
 including 1), GQA group size, head dim, window (including 1 and >= T), scale,
 and sink logits drawn from finite values and +-inf; prefill and verify (random
-history lengths and 1..4 draft rows).  Examples are derandomized, so every run
-checks the same cases.  CPU only."""
+history lengths and 1..4 draft rows).  The oracle's gradients are checked the
+same way against torch's fp64 autograd of a plain torch forward.  Examples are
+derandomized, so every run checks the same cases.  CPU only."""
 import math
 
 import numpy as np
@@ -86,3 +87,46 @@ def test_verify_oracle_equals_brute_force(case):
     o = oracle.verify(q, cu_q, k_hist, v_hist, seq_lens, sink, window, sc)
     ob = brute.verify(q, cu_q, k_hist, v_hist, seq_lens, sink, window, sc)
     np.testing.assert_allclose(o, ob, rtol=0, atol=1e-11)
+
+
+@st.composite
+def backward_case(draw):
+    B = draw(st.integers(1, 2))
+    T = draw(st.integers(1, 12))
+    Hkv = draw(st.sampled_from([1, 2]))
+    G = draw(st.sampled_from([1, 2, 4]))
+    D = draw(st.sampled_from([4, 8]))
+    window = draw(st.one_of(st.none(), st.integers(1, 14)))
+    sinks = draw(st.lists(st.one_of(st.floats(-4.0, 4.0), st.just(-math.inf)),
+                          min_size=Hkv * G, max_size=Hkv * G))
+    seed = draw(st.integers(0, 2**31 - 1))
+    return B, T, Hkv * G, Hkv, D, window, sinks, seed
+
+
+@settings(max_examples=40, deadline=None, derandomize=True,
+          suppress_health_check=[HealthCheck.too_slow])
+@given(backward_case())
+def test_backward_oracle_equals_torch_autograd(case):
+    """The oracle's gradients (dq, dk, dv, dsink) against torch's fp64 autograd
+    of a plain torch forward (masked scores, a sink column, library softmax)."""
+    import torch
+    from oracle import backward
+    B, T, Hq, Hkv, D, window, sinks, seed = case
+    rng = np.random.default_rng(seed)
+    q, do = (rng.standard_normal((B, T, Hq, D)) for _ in range(2))
+    k, v = (rng.standard_normal((B, T, Hkv, D)) for _ in range(2))
+    sink = np.asarray(sinks, np.float64)
+    ours = backward.prefill_backward(q, k, v, sink, do, window)
+    tq, tk, tv, ts = (torch.tensor(x, requires_grad=True) for x in (q, k, v, sink))
+    G = Hq // Hkv
+    s = torch.einsum("bihd,bjhd->bhij", tq, tk.repeat_interleave(G, dim=2)) / math.sqrt(D)
+    i, j = torch.arange(T)[:, None], torch.arange(T)[None, :]
+    vis = (j <= i) & ((j > i - window) if window else torch.ones(T, T, dtype=torch.bool))
+    s = s.masked_fill(~vis, -math.inf)
+    col = ts.view(1, Hq, 1, 1).expand(B, Hq, T, 1)
+    p = torch.softmax(torch.cat([s, col], dim=-1), dim=-1)[..., :T]
+    o = torch.einsum("bhij,bjhd->bihd", p, tv.repeat_interleave(G, dim=2))
+    (o * torch.tensor(do)).sum().backward()
+    ref = (tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy(), ts.grad.numpy())
+    for name, a, b in zip(("dq", "dk", "dv", "dsink"), ours, ref):
+        np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-11, err_msg=name)
