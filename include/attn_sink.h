@@ -56,7 +56,10 @@
  *   - errors only the device can see (a page id outside the pool, a sequence
  *     longer than the cache, q_len > q_max, a pipeline wait that timed out)
  *     set bits in a device error word, the offending work is skipped (never a
- *     trap), and attn_check_device_error() reports them.
+ *     trap), and attn_check_device_error() reports them;
+ *   - while ATTN_DEVERR_WAIT_TIMEOUT is set, kernels launched by this library
+ *     return without doing any work, so a stalled pipeline is not run into
+ *     again; attn_check_device_error() clears the word.
  */
 #ifndef ATTN_SINK_H
 #define ATTN_SINK_H
