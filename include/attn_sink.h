@@ -57,9 +57,11 @@
  *     longer than the cache, q_len > q_max, a pipeline wait that timed out)
  *     set bits in a device error word, the offending work is skipped (never a
  *     trap), and attn_check_device_error() reports them;
- *   - while ATTN_DEVERR_WAIT_TIMEOUT is set, kernels launched by this library
- *     return without doing any work, so a stalled pipeline is not run into
- *     again; attn_check_device_error() clears the word.
+ *   - while ATTN_DEVERR_WAIT_TIMEOUT is set, the pipelined kernels (the
+ *     tensor-core prefill and the verify kernels, the ones with bounded
+ *     barrier waits) return without doing any work, so a stalled pipeline is
+ *     not run into again; the fp32 prefill, the appends and the backward run
+ *     as usual.  attn_check_device_error() clears the word.
  */
 #ifndef ATTN_SINK_H
 #define ATTN_SINK_H
@@ -313,8 +315,9 @@ attn_status_t attn_debug_verify_positions(int32_t *out, int kind, const int32_t 
 /* attn_debug_wait_timeout: enqueues one kernel whose only pipeline wait (an
  * mbarrier phase that nothing completes) runs out after the kernels' wait
  * limit of 2 s and sets ATTN_DEVERR_WAIT_TIMEOUT in the device error word, as
- * a stalled pipeline would.  Kernels launched while that bit is set return
- * without doing any work; attn_check_device_error() reports and clears it.
+ * a stalled pipeline would.  Pipelined kernels launched while that bit is set
+ * (tensor-core prefill, verify) return without doing any work;
+ * attn_check_device_error() reports and clears it.
  * For tests of the failure path: no trap, no fault, and the context stays
  * usable.  Errors: ATTN_ERR_CUDA if no device is current or the launch fails. */
 attn_status_t attn_debug_wait_timeout(void *stream);
