@@ -56,3 +56,30 @@ def test_clock_sampler_parses_nvidia_smi_lines():
 def test_clock_sampler_without_samples_reports_none():
     out = bench.ClockSampler(0).summary()
     assert out["sm_mhz"] is None and out["reasons"] == [] and out["samples"] == 0
+
+
+def test_traffic_record_is_used_only_for_the_source_it_was_taken_on(tmp_path, monkeypatch):
+    """Recorded DRAM counters count for the headline only while the kernel file
+    and the library headers are unchanged; a changed source gives null."""
+    rel = "global_attention_sinks_swa_b300/csrc/prefill_swa.cu"
+    assert bench.source_sha(rel) == bench.source_sha(rel)
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    entry = rec["prefill_swa_stream_kernel"]
+    assert bench.ncu_traffic(rel, "prefill_swa_stream_kernel") == (
+        float(entry["dram_bytes_per_launch"]) if entry["source_sha"] == bench.source_sha(rel)
+        else None)
+    # a copy of the tree whose kernel file differs by one byte: the record is stale
+    root = tmp_path / "tree"
+    csrc = root / "global_attention_sinks_swa_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    (root / "profiles").mkdir()
+    src_dir = os.path.join(ROOT, "global_attention_sinks_swa_b300", "csrc")
+    for f in os.listdir(src_dir):
+        data = open(os.path.join(src_dir, f), "rb").read()
+        if f == "prefill_swa.cu":
+            data += b"\n"
+        (csrc / f).write_bytes(data)
+    (root / "profiles" / "traffic.json").write_text(json.dumps(
+        {"prefill_swa_stream_kernel": dict(entry, source_sha=bench.source_sha(rel))}))
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.ncu_traffic(rel, "prefill_swa_stream_kernel") is None
