@@ -574,11 +574,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Split-KV merge for the paged cache: per (request, kv head), combine the
 // splits' (m, l, o) by log-sum-exp and add the sink term once:
 //   M = max(sigma, m_s),  o = sum_s 2^(m_s-M) o_s / (2^(sigma-M) + sum_s 2^(m_s-M) l_s)
+// A split CTA whose pipeline wait ran out leaves its partials unwritten and
+// sets ATTN_DEVERR_WAIT_TIMEOUT before this kernel starts (stream order), as
+// does an earlier launch that timed out; the merge then writes nothing, so no
+// output is ever made from scratch that this call did not write.
 __global__ void __launch_bounds__(256)
     verify_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_ml,
                           const int32_t *__restrict__ cu_q, const int32_t *__restrict__ seq_lens,
                           const float *__restrict__ sink, __nv_bfloat16 *__restrict__ o,
-                          int nsplit, int Hq, int Hkv, int q_max, int max_ctx, int max_pages) {
+                          int nsplit, int Hq, int Hkv, int q_max, int max_ctx, int max_pages,
+                          const unsigned *err) {
+    if (ptx::prior_timeout(err)) return;
     const int g = blockIdx.x, b = blockIdx.y;
     const int G = Hq / Hkv;
     const int r0 = cu_q[b], q_len = cu_q[b + 1] - r0, L = seq_lens[b];
@@ -669,7 +675,7 @@ cudaError_t launch_verify_paged(const VerifyMaps &maps, const void *q, const int
     if (e != cudaSuccess || finalize) return e;
     verify_combine_kernel<<<dim3(Hkv, B), 256, 0, s>>>(ws_o, ws_ml, cu_q, seq_lens, sink,
                                                        static_cast<__nv_bfloat16 *>(o), nsplit, Hq,
-                                                       Hkv, q_max, max_ctx, max_pages);
+                                                       Hkv, q_max, max_ctx, max_pages, err);
     return cudaGetLastError();
 }
 

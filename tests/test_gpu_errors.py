@@ -89,3 +89,48 @@ def test_host_side_errors_return_status():
                                torch.tensor([10], dtype=torch.int32, device="cuda"), sink,
                                window=128, q_max=4)
     assert e.value.status == A.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("entry", ["workspace", "noalloc"])
+def test_wait_timeout_skips_split_verify_and_its_merge(entry):
+    """Contexts longer than one 4096-token split run the split-KV merge kernel.
+    A first call fills the split scratch with valid partials; with the timeout
+    bit set, a second call must leave its output untouched rather than merge
+    whatever the scratch still holds."""
+    _clear()
+    ctx = np.array([9000, 5000], np.int32)
+    npages = (ctx + 63) // 64
+    num_pages = int(npages.sum())
+    pt = np.zeros((2, int(npages.max())), np.int32)
+    pt[0, :npages[0]] = np.arange(npages[0])
+    pt[1, :npages[1]] = npages[0] + np.arange(npages[1])
+    kp = synth.normal((num_pages, Hkv, 64, D), 31, device="cuda")
+    vp = synth.normal((num_pages, Hkv, 64, D), 32, device="cuda")
+    cu_q = torch.tensor([0, 4, 7], dtype=torch.int32, device="cuda")
+    q = synth.normal((7, Hq, D), 33, device="cuda")
+    sink = synth.sink_logits(Hq, 34, device="cuda")
+    args = (q, cu_q, kp, vp, torch.from_numpy(pt).cuda(), torch.from_numpy(ctx).cuda(), sink)
+    max_ctx = 12000   # three splits
+    assert A.attn_ga_sink_verify_workspace(2, Hq, Hkv, D, 4, max_ctx) > 0
+    ws = torch.empty(A.attn_ga_sink_verify_workspace(2, Hq, Hkv, D, 4, max_ctx),
+                     dtype=torch.uint8, device="cuda")
+
+    def call(out):
+        if entry == "workspace":
+            A.attn_ga_sink_verify(*args, max_ctx=max_ctx, q_max=4, out=out, workspace=ws)
+        else:
+            A.attn_ga_sink_verify_noalloc(*args, max_ctx=max_ctx, q_max=4, out=out)
+
+    good = torch.empty_like(q)
+    call(good)   # leaves valid partials in the scratch
+    assert A.attn_check_device_error() == 0
+    assert torch.isfinite(good.float()).all()
+    A.attn_debug_wait_timeout()
+    o = torch.full_like(q, float("nan"))
+    call(o)
+    assert A.attn_check_device_error() & A.DEVERR_WAIT_TIMEOUT
+    assert torch.isnan(o.float()).all()   # neither the splits nor the merge wrote anything
+    o2 = torch.full_like(q, float("nan"))
+    call(o2)   # the word was cleared: the same call computes again
+    assert A.attn_check_device_error() == 0
+    assert torch.equal(o2, good)

@@ -193,17 +193,20 @@ def test_appends_bit_exact():
 
 
 def test_mtp_walk_sequence():
-    """A synthetic MTP loop: each pass appends 1 real + up to 3 draft tokens
-    through the append kernels, verifies them against the ring and the pages,
-    then accepts a random prefix and rolls the length back (the next append
-    overwrites the rejected slots).  Every pass matches the oracle on the
+    """A synthetic MTP loop of 200 passes: each pass appends 1 real + up to 3
+    draft tokens per request through the append kernels, verifies them against
+    the ring and the pages, then accepts a random prefix per request (drawn
+    per pass and request) and rolls the length back, so the next append
+    overwrites the rejected slots.  Every pass matches the oracle on the
     linear history."""
-    B, steps = 3, 40
+    B, steps = 3, 200
     L0 = np.array([0, 127, 4090], np.int32)
     Lcap = int(L0.max()) + steps * QMAX + 8
-    rng = np.random.default_rng(0)
     k_hist = synth.normal((B, Lcap, Hkv, D), 100)
     v_hist = synth.normal((B, Lcap, Hkv, D), 101)
+    # fp32 copies (exact) for the oracle, kept in step with the bf16 history
+    k32 = k_hist.float().numpy().copy()
+    v32 = v_hist.float().numpy().copy()
     sink = synth.sink_logits(Hq, 102)
     max_pages = (Lcap + PAGE - 1) // PAGE
     num_pages = B * max_pages
@@ -214,7 +217,8 @@ def test_mtp_walk_sequence():
     kp = pages_from_history(k_hist, hist0, page_table, num_pages).cuda()
     vp = pages_from_history(v_hist, hist0, page_table, num_pages).cuda()
     pt = torch.from_numpy(page_table).cuda()
-    accepts = synth.accept_counts(steps, QMAX, 104)
+    accepts = synth.accept_counts(steps * B, QMAX, 104).reshape(steps, B)
+    sink_d = sink.cuda()
     base = L0.copy()
     for s in range(steps):
         q_lens = np.array([QMAX if (s + b) % 7 else 1 + (s % QMAX) for b in range(B)], np.int32)
@@ -224,23 +228,22 @@ def test_mtp_walk_sequence():
         k_new = synth.normal((int(cu_q[-1]), Hkv, D), 1000 + s)
         v_new = synth.normal((int(cu_q[-1]), Hkv, D), 2000 + s)
         for b in range(B):
-            k_hist[b, base[b]:seq_lens[b]] = k_new[cu_q[b]:cu_q[b + 1]]
-            v_hist[b, base[b]:seq_lens[b]] = v_new[cu_q[b]:cu_q[b + 1]]
+            k32[b, base[b]:seq_lens[b]] = k_new[cu_q[b]:cu_q[b + 1]].float().numpy()
+            v32[b, base[b]:seq_lens[b]] = v_new[cu_q[b]:cu_q[b + 1]].float().numpy()
         cu, sl = torch.from_numpy(cu_q).cuda(), torch.from_numpy(seq_lens).cuda()
         A.attn_swa_ring_append(k_new.cuda(), v_new.cuda(), cu, sl, ring_k, ring_v, q_max=QMAX)
         A.attn_ga_paged_append(k_new.cuda(), v_new.cuda(), cu, sl, kp, vp, pt, q_max=QMAX)
         q = synth.normal((int(cu_q[-1]), Hq, D), 3000 + s)
-        o_ring = A.attn_swa_sink_verify(q.cuda(), cu, ring_k, ring_v, sl, sink.cuda(), window=W,
+        o_ring = A.attn_swa_sink_verify(q.cuda(), cu, ring_k, ring_v, sl, sink_d, window=W,
                                         q_max=QMAX)
-        o_pg = A.attn_ga_sink_verify(q.cuda(), cu, kp, vp, pt, sl, sink.cuda(), max_ctx=Lcap,
+        o_pg = A.attn_ga_sink_verify(q.cuda(), cu, kp, vp, pt, sl, sink_d, max_ctx=Lcap,
                                      q_max=QMAX)
         assert A.attn_check_device_error() == 0
-        assert_bf16_close(o_ring, oracle.verify(q, cu_q, k_hist, v_hist, seq_lens, sink, W),
+        assert_bf16_close(o_ring, oracle.verify(q, cu_q, k32, v32, seq_lens, sink, W),
                           f"ring step {s}")
-        assert_bf16_close(o_pg, oracle.verify(q, cu_q, k_hist, v_hist, seq_lens, sink, None),
+        assert_bf16_close(o_pg, oracle.verify(q, cu_q, k32, v32, seq_lens, sink, None),
                           f"paged step {s}")
-        acc = np.minimum(accepts[s] + rng.integers(0, 2, B), q_lens - 1)
-        base = base + 1 + acc
+        base = base + 1 + np.minimum(accepts[s], q_lens - 1)
 
 
 # ------------------------------------------------------- full sizes, sampled
@@ -296,3 +299,28 @@ def test_full_size_verify_sampled(name):
         r = oracle.verify(q[r0:r1].cpu(), np.array([0, r1 - r0], np.int32), kh, vh,
                           np.array([L], np.int32), sink.cpu(), None)
         assert_bf16_close(o[r0:r1], r, f"{name} request {b}")
+
+
+def test_full_size_ring_verify_all_requests():
+    """The ring verify at the measured configuration: 64 requests x 4 tokens,
+    contexts ~ U[4096, 65536], 131-slot rings filled on the device.  The
+    queries see only the last 131 positions, so each request's history for
+    the oracle is its ring read out in position order (positions L-131..L-1,
+    re-based to 0..130, which keeps every query-key distance)."""
+    nreq = 64
+    ctx = synth.context_lengths(nreq, 4096, 65536, 2099)
+    q_lens = np.full(nreq, QMAX, np.int32)
+    cu_q = synth.cu_seqlens(q_lens)
+    rk = synth.normal((nreq, Hkv, R, D), 2004, device="cuda")
+    rv = synth.normal((nreq, Hkv, R, D), 2005, device="cuda")
+    q = synth.normal((nreq * QMAX, Hq, D), 2104, device="cuda")
+    sink = synth.sink_logits(Hq, 2105, device="cuda")
+    o = A.attn_swa_sink_verify(q, torch.from_numpy(cu_q).cuda(), rk, rv,
+                               torch.from_numpy(ctx).cuda(), sink, window=W, q_max=QMAX)
+    assert A.attn_check_device_error() == 0
+    order = np.stack([(int(L) - R + np.arange(R)) % R for L in ctx])   # slot of position L-R+j
+    idx = torch.from_numpy(order).long().cuda()
+    kh = torch.stack([rk[b][:, idx[b]] for b in range(nreq)]).transpose(1, 2).cpu()
+    vh = torch.stack([rv[b][:, idx[b]] for b in range(nreq)]).transpose(1, 2).cpu()
+    ref_o = oracle.verify(q.cpu(), cu_q, kh, vh, np.full(nreq, R, np.int32), sink.cpu(), W)
+    assert_bf16_close(o, ref_o, "ring verify, 64 requests x q4")
