@@ -8,6 +8,26 @@
 
 namespace attn {
 
+// Launches `kernel` with programmatic stream serialization: it may begin while
+// the preceding kernel of the stream is still running (once that kernel lets
+// dependents launch), so every kernel launched this way calls
+// ptx::grid_dep_wait() before it reads or writes global memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Sequences of a prefill batch: B sequences of T tokens each (cu == nullptr,
 // total = B*T), or B packed sequences given by the device array cu[B+1] with
 // cu[B] = total tokens and T >= the longest one (T sizes grids only).
@@ -83,9 +103,11 @@ constexpr int kVerifyRows = 32;       // q_max * G rows per (request, kv head), 
 constexpr int kVerifyBlock = 64;      // keys per pipeline stage (one GA page)
 constexpr int kVerifyChunkPages = 64; // pages per split of the GA context (4096 tokens)
 
-// tcgen05 ring verify: one CTA per (request, kv head), the whole ring in one
-// pass; K/V maps with a box of kVerifyRingKeys slot rows.
+// tcgen05 ring verify: persistent CTAs over (request, kv head) units, the
+// whole ring of a unit in one pass; K/V maps with a box of kVerifyRingKeys
+// slot rows.
 constexpr int kVerifyRingKeys = 144;  // ring slots covered (R <= 144), multiple of 16
+constexpr int kVerifyRingUnitsPerCta = 64;  // (request, kv head) units per persistent CTA, at most
 int verify_ring_tc_supported(int G, int R, int q_max);
 cudaError_t launch_verify_ring_tc(const VerifyMaps &maps, const int32_t *cu_q,
                                   const int32_t *seq_lens, const float *sink, void *o, int B,

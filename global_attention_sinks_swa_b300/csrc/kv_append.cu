@@ -6,7 +6,10 @@
 // verify pass (figure "Multi-Token Prediction": 1 real + 3 draft tokens).
 //
 // One block per (request, new-token index); each thread copies 16-byte
-// vectors.  Bad indices set a device error bit and skip the copy.
+// vectors.  Bad indices set a device error bit and skip the copy.  Launched as
+// programmatic dependents: a block waits for the preceding kernel's memory
+// before its first global access, then lets the next kernel (a verify that
+// prefetches its cache while this copy runs) launch.
 #include <cuda_bf16.h>
 
 #include "index_math.cuh"
@@ -40,6 +43,8 @@ __global__ void ring_append_kernel(const uint4 *__restrict__ k_new, const uint4 
                                    const int32_t *__restrict__ seq_lens, uint4 *__restrict__ ring_k,
                                    uint4 *__restrict__ ring_v, int Hkv, int vecs_per_row, int R,
                                    int q_max, unsigned *err) {
+    ptx::grid_dep_wait();  // the preceding kernel's writes are visible from here on
+    ptx::grid_dep_launch_dependents();
     const int b = blockIdx.x, t = blockIdx.y;
     int row, pos;
     if (!request_token(cu_q, seq_lens, b, t, q_max, err, &row, &pos)) return;
@@ -62,6 +67,8 @@ __global__ void paged_append_kernel(const uint4 *__restrict__ k_new,
                                     const int32_t *__restrict__ page_table, int max_pages,
                                     int num_pages, int page_size, int Hkv, int vecs_per_row,
                                     int q_max, unsigned *err) {
+    ptx::grid_dep_wait();  // the preceding kernel's writes are visible from here on
+    ptx::grid_dep_launch_dependents();
     const int b = blockIdx.x, t = blockIdx.y;
     int row, pos;
     if (!request_token(cu_q, seq_lens, b, t, q_max, err, &row, &pos)) return;
@@ -98,6 +105,8 @@ __global__ void paged_append_fp8_kernel(const uint4 *__restrict__ k_new,
                                         const float *__restrict__ k_scale,
                                         const float *__restrict__ v_scale, int Hkv, int q_max,
                                         unsigned *err) {
+    ptx::grid_dep_wait();  // the preceding kernel's writes are visible from here on
+    ptx::grid_dep_launch_dependents();
     const int b = blockIdx.x, t = blockIdx.y;
     int row, pos;
     if (!request_token(cu_q, seq_lens, b, t, q_max, err, &row, &pos)) return;
@@ -145,10 +154,10 @@ cudaError_t launch_ring_append(const void *k_new, const void *v_new, const int32
                                cudaStream_t s) {
     if (B == 0 || q_max == 0) return cudaSuccess;
     const int vpr = D * elem_bytes / 16;
-    ring_append_kernel<<<dim3(B, q_max), 128, 0, s>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), cu_q, seq_lens,
-        static_cast<uint4 *>(ring_k), static_cast<uint4 *>(ring_v), Hkv, vpr, R, q_max, err);
-    return cudaGetLastError();
+    return launch_pdl(ring_append_kernel, dim3(B, q_max), dim3(128), 0, s,
+                      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), cu_q,
+                      seq_lens, static_cast<uint4 *>(ring_k), static_cast<uint4 *>(ring_v), Hkv,
+                      vpr, R, q_max, err);
 }
 
 cudaError_t launch_paged_append(const void *k_new, const void *v_new, const int32_t *cu_q,
@@ -158,11 +167,10 @@ cudaError_t launch_paged_append(const void *k_new, const void *v_new, const int3
                                 unsigned int *err, cudaStream_t s) {
     if (B == 0 || q_max == 0) return cudaSuccess;
     const int vpr = D * elem_bytes / 16;
-    paged_append_kernel<<<dim3(B, q_max), 128, 0, s>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), cu_q, seq_lens,
-        static_cast<uint4 *>(k_pages), static_cast<uint4 *>(v_pages), page_table, max_pages,
-        num_pages, page_size, Hkv, vpr, q_max, err);
-    return cudaGetLastError();
+    return launch_pdl(paged_append_kernel, dim3(B, q_max), dim3(128), 0, s,
+                      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), cu_q,
+                      seq_lens, static_cast<uint4 *>(k_pages), static_cast<uint4 *>(v_pages),
+                      page_table, max_pages, num_pages, page_size, Hkv, vpr, q_max, err);
 }
 
 }  // namespace attn
@@ -175,11 +183,11 @@ cudaError_t launch_paged_append_fp8(const void *k_new, const void *v_new, const 
                                     int page_size, const float *k_scale, const float *v_scale,
                                     int B, int Hkv, int q_max, unsigned int *err, cudaStream_t s) {
     if (B == 0 || q_max == 0) return cudaSuccess;
-    paged_append_fp8_kernel<<<dim3(B, q_max), 128, 0, s>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), cu_q, seq_lens,
-        static_cast<uint4 *>(k_pages), static_cast<uint4 *>(v_pages), page_table, max_pages,
-        num_pages, page_size, k_scale, v_scale, Hkv, q_max, err);
-    return cudaGetLastError();
+    return launch_pdl(paged_append_fp8_kernel, dim3(B, q_max), dim3(128), 0, s,
+                      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), cu_q,
+                      seq_lens, static_cast<uint4 *>(k_pages), static_cast<uint4 *>(v_pages),
+                      page_table, max_pages, num_pages, page_size, k_scale, v_scale, Hkv, q_max,
+                      err);
 }
 
 }  // namespace attn

@@ -41,6 +41,13 @@ ATTN_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
                  "r"(bytes)
                  : "memory");
 }
+// Adds `bytes` to the transaction count of the current phase without arriving
+// (the phase still needs its arrivals).
+ATTN_DEV void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
 ATTN_DEV void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -49,6 +56,20 @@ ATTN_DEV bool mbar_test(uint32_t addr, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred P;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P;\n}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Non-blocking probe of the phase with parity `parity` (mbarrier.test_wait
+// never suspends the thread, unlike try_wait): for loops that poll several
+// barriers and must act on whichever completes first.
+ATTN_DEV bool mbar_poll(uint32_t addr, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
         "selp.b32 %0, 1, 0, P;\n}"
         : "=r"(done)
         : "r"(addr), "r"(parity)
@@ -112,6 +133,27 @@ ATTN_DEV void tma_store_3d(const void *tmap, const void *src, int c0, int c1, in
         "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// Brings a tensor-map box into L2 only (no shared memory, no completion to
+// wait for).  A hint: the data stays coherent whatever writes it later.
+ATTN_DEV void tma_prefetch_l2_4d(const void *tmap, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// ------------------------------------------ programmatic dependent launch
+// Blocks until every grid this one depends on (the preceding kernel of the
+// stream when launched with programmatic stream serialization) has completed
+// and its memory operations are visible; returns at once otherwise.
+ATTN_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel of the stream, if launched with programmatic stream
+// serialization, begin before this grid ends (it still waits in
+// grid_dep_wait() for this grid's memory before using it).
+ATTN_DEV void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Ampere-style asynchronous copies (16 or 4 bytes); src_bytes = 0 fills zeros
 // and reads nothing.
 ATTN_DEV void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
