@@ -484,6 +484,105 @@ def bench_verify_swa(A, nreq, steps, warmup, world, stream, seed):
     return ms, kv
 
 
+# ------------------------------------------------- one MTP step, model order
+def model_step_problem(A, nreq, lo, hi, seed, q_lens=None, ctx=None):
+    """The attention of one MTP verify step over the 48-layer hybrid stack in
+    model order (synth.hybrid_layer_kinds: GA at layers 0, 5, 11, .., 47):
+    every layer owns its cache (a 131-slot ring per SWA layer, a paged pool
+    per GA layer), its queries, its new keys/values and its sink logits.
+    nreq requests with contexts ~ U[lo, hi] (seeded), 4 new tokens each
+    unless q_lens is given (contexts too, when ctx is given)."""
+    import torch
+    import synth
+    kinds = synth.hybrid_layer_kinds()
+    ctx = (synth.context_lengths(nreq, lo, hi, seed) if ctx is None
+           else np.asarray(ctx, np.int32))
+    q_lens = np.full(nreq, QMAX, np.int32) if q_lens is None else np.asarray(q_lens, np.int32)
+    cu_q = synth.cu_seqlens(q_lens)
+    nq = int(cu_q[-1])
+    npages = (ctx + PAGE - 1) // PAGE
+    num_pages, max_pages = int(npages.sum()), int(npages.max())
+    layers = []
+    for li, kind in enumerate(kinds):
+        base = seed + 1000 * (li + 1)
+        d = {"kind": kind,
+             "q": synth.normal((nq, HQ, D), base, device="cuda"),
+             "k_new": synth.normal((nq, HKV, D), base + 1, device="cuda"),
+             "v_new": synth.normal((nq, HKV, D), base + 2, device="cuda"),
+             "sink": synth.sink_logits(HQ, base + 3, device="cuda"),
+             "out": torch.empty(nq, HQ, D, dtype=torch.bfloat16, device="cuda")}
+        if kind == "swa":
+            d["rk"] = synth.normal((nreq, HKV, RING, D), base + 4, device="cuda")
+            d["rv"] = synth.normal((nreq, HKV, RING, D), base + 5, device="cuda")
+        else:
+            perm = synth.page_permutation(num_pages, base + 6)
+            pt = np.zeros((nreq, max_pages), np.int32)
+            o = 0
+            for b in range(nreq):
+                pt[b, :npages[b]] = perm[o:o + npages[b]]
+                o += npages[b]
+            d["pt"] = torch.from_numpy(pt).cuda()
+            d["kp"] = synth.normal((num_pages, HKV, PAGE, D), base + 7, device="cuda")
+            d["vp"] = synth.normal((num_pages, HKV, PAGE, D), base + 8, device="cuda")
+        layers.append(d)
+    max_ctx = int(ctx.max())
+    ws_bytes = A.attn_ga_sink_verify_workspace(nreq, HQ, HKV, D, QMAX, max_ctx)
+    return {"layers": layers, "ctx": ctx, "q_lens": q_lens, "cu_q_np": cu_q,
+            "cu_q": torch.from_numpy(cu_q).cuda(), "seq_lens": torch.from_numpy(ctx).cuda(),
+            "max_ctx": max_ctx,
+            "ws": torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")}
+
+
+def model_step(A, P, stream):
+    """Enqueue the step: for each layer in order, append its new keys/values
+    to its cache, then verify.  Every kernel is launched as a programmatic
+    dependent of the one before it, so a layer's verify can set up and
+    prefetch its cache into L2 while the previous kernel finishes."""
+    cu, sl = P["cu_q"], P["seq_lens"]
+    for d in P["layers"]:
+        if d["kind"] == "swa":
+            A.attn_swa_ring_append(d["k_new"], d["v_new"], cu, sl, d["rk"], d["rv"], q_max=QMAX,
+                                   stream=stream)
+            A.attn_swa_sink_verify(d["q"], cu, d["rk"], d["rv"], sl, d["sink"], window=W,
+                                   q_max=QMAX, out=d["out"], stream=stream)
+        else:
+            A.attn_ga_paged_append(d["k_new"], d["v_new"], cu, sl, d["kp"], d["vp"], d["pt"],
+                                   q_max=QMAX, stream=stream)
+            A.attn_ga_sink_verify(d["q"], cu, d["kp"], d["vp"], d["pt"], sl, d["sink"],
+                                  max_ctx=P["max_ctx"], q_max=QMAX, out=d["out"],
+                                  workspace=P["ws"], stream=stream)
+
+
+def model_step_kv_bytes(P) -> float:
+    """K+V bytes the step's verifies read: the ring of every SWA layer and the
+    visible pages of every GA layer, once per (request, kv head)."""
+    n_swa = sum(d["kind"] == "swa" for d in P["layers"])
+    n_ga = len(P["layers"]) - n_swa
+    return n_swa * float(len(P["ctx"])) * RING * HKV * D * 2 * 2 + n_ga * verify_kv_bytes(P["ctx"])
+
+
+def bench_verify_step(A, nreq, steps, warmup, world, stream, seed):
+    """One MTP step over the 48 layers (39 SWA ring + 9 GA paged verifies, each
+    after its cache append) replayed as one CUDA graph."""
+    import torch
+    P = model_step_problem(A, nreq, 4096, 65536, seed)
+    with torch.cuda.stream(stream):
+        model_step(A, P, stream)   # warm (tensor-map encode, function attributes)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            model_step(A, P, stream)
+        for _ in range(warmup):
+            graph.replay()
+        ms = time_region(lambda _: graph.replay(), steps, world, stream)
+    if A.attn_check_device_error(stream) != 0:
+        raise RuntimeError("model step reported a device error")
+    kv = model_step_kv_bytes(P)
+    del P, graph
+    torch.cuda.empty_cache()
+    return ms, kv
+
+
 # --------------------------------------------------------------- CPU baseline
 def cpu_baseline(seconds_target: float = 15.0):
     """The fp64 oracle on a bounded sample of the headline workload (rows of
@@ -519,7 +618,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-parts", action="store_true", help="headline only")
     ap.add_argument("--profile", default="",
-                    help="comma list of swa,ga,verify_ga,verify_ga_fp8,verify_swa,backward: run only these kernels "
+                    help="comma list of swa,ga,verify_ga,verify_ga_fp8,verify_swa,verify_step,backward: run only these kernels "
                          "(warmup + steps), no JSON line; for ncu captures")
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -601,6 +700,17 @@ def main():
             "ms_per_39_layers": ms_s,
             "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
                          "frac": kv_s / (ms_s * 1e-3) / 1e9 / hbm}}
+        torch.cuda.empty_cache()
+        ms_st, kv_st = bench_verify_step(A, 64, max(3, args.steps // 5), warmup, world, stream,
+                                         3004 + 10 * rank)
+        parts["verify_step_48layers"] = {
+            "config": "one MTP step in model order: 48 layers (GA at 0,5,11,..,47; 39 SWA ring + "
+                      "9 GA paged), append + verify per layer, 64 req x q4, ctx~U[4096,65536], "
+                      "distinct caches, one CUDA graph, programmatic dependent launches",
+            "value": kv_st / (ms_st * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_st,
+            "layers_per_s": 48 * 1e3 / ms_st, "kv_bytes_per_step": kv_st,
+            "roofline": {"bound": "hbm", "peak": hbm, "unit": "GB/s",
+                         "frac": kv_st / (ms_st * 1e-3) / 1e9 / hbm}}
         for ql, name in ((4, "verify_ga_8x262144_q4"), (1, "verify_ga_8x262144_q1")):
             ctx5 = np.full(8, 262144, np.int32)
             ms5, kv5 = bench_verify_ga(A, ctx5, np.full(8, ql, np.int32), args.steps, warmup, world,
@@ -669,6 +779,8 @@ def run_profile(A, synth, args, warmup, stream):
                             fp8=name.endswith("fp8"))
         elif name == "verify_swa":
             bench_verify_swa(A, 64, args.steps, warmup, 1, stream, 2004)
+        elif name == "verify_step":
+            bench_verify_step(A, 64, args.steps, warmup, 1, stream, 3004)
         else:
             raise SystemExit(f"unknown profile target {name}")
     print(json.dumps({"profile": args.profile, "ok": True}), flush=True)

@@ -109,3 +109,14 @@ def history(L: int, Hkv: int, D: int, seed: int, dtype=torch.bfloat16, device="c
 def cu_seqlens(q_lens) -> np.ndarray:
     q_lens = np.asarray(q_lens, dtype=np.int64)
     return np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+
+
+def hybrid_layer_kinds(blocks: int = 8, swa_per_block: int = 5) -> list[str]:
+    """Attention kind of each layer of the hybrid stack, in model order: M = 8
+    blocks of 5 SWA layers followed by one GA layer, where the first layer of
+    the stack is GA instead of SWA (technical-report summary, section
+    "MiMo-V2-Flash Model Architecture", and its hyper-parameter paragraph:
+    48 layers, 39 SWA and 9 GA).  A workload shape, not arithmetic."""
+    kinds = (["swa"] * swa_per_block + ["ga"]) * blocks
+    kinds[0] = "ga"
+    return kinds
