@@ -262,8 +262,18 @@ ATTN_EXPORT attn_status_t attn_sink_prefill_backward(
         return fail(ATTN_ERR_INVALID_ARG, "workspace too small: need %zu bytes", need);
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    cudaError_t e = attn::launch_prefill_backward(q, k, v, o, lse, dout, sink, dq, dk, dv, dsink,
-                                                  workspace, B, T, Hq, Hkv, window, scale,
+    unsigned *err = device_error_word();
+    if (!err) return fail(ATTN_ERR_CUDA, "no CUDA device / error word unavailable");
+    attn::BwdMaps maps;
+    const uint64_t rows = static_cast<uint64_t>(B) * T;
+    if (B > 0 && T > 0 &&
+        !(map_3d(&maps.q_rows64, q, rows, Hq, 1, 64) && map_3d(&maps.dout_rows64, dout, rows, Hq, 1, 64) &&
+          map_3d(&maps.k_rows128, k, rows, Hkv, 1, 128) && map_3d(&maps.v_rows128, v, rows, Hkv, 1, 128) &&
+          map_3d(&maps.q_rows128, q, rows, Hq, 1, 128) && map_3d(&maps.dout_rows128, dout, rows, Hq, 1, 128) &&
+          map_3d(&maps.k_rows64, k, rows, Hkv, 1, 64) && map_3d(&maps.v_rows64, v, rows, Hkv, 1, 64)))
+        return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward maps");
+    cudaError_t e = attn::launch_prefill_backward(maps, o, lse, dout, sink, dq, dk, dv, dsink,
+                                                  workspace, B, T, Hq, Hkv, window, scale, err,
                                                   as_stream(stream));
     return e == cudaSuccess ? ok() : cuda_fail(e, "backward launch");
 }

@@ -119,6 +119,32 @@ ATTN_HD bool ga_tile_needs_mask(int q0, int j, int window) {
     return false;
 }
 
+// ---- backward tiling.  The dK/dV kernel owns keys j0..j0+bk-1 and visits the
+// query tiles of bq rows [first, last] holding a row that sees one of them;
+// the dQ kernel owns query rows i0..i0+bq-1 and visits the key tiles of bk
+// keys [first, last] holding a key one of its rows sees (window <= 0: causal).
+ATTN_HD void bwd_kv_query_tiles(int j0, int T, int window, int bk, int bq, int *first, int *last) {
+    *first = j0 / bq;
+    int hi = T - 1;
+    if (window > 0 && j0 + bk - 1 + window - 1 < hi) hi = j0 + bk - 1 + window - 1;
+    *last = hi / bq;
+}
+ATTN_HD void bwd_q_key_tiles(int i0, int T, int window, int bq, int bk, int *first, int *last) {
+    int lo = window > 0 ? i0 - window + 1 : 0;
+    if (lo < 0) lo = 0;
+    *first = lo / bk;
+    int hi = i0 + bq - 1;
+    if (hi > T - 1) hi = T - 1;
+    *last = hi / bk;
+}
+// True when every pair of query rows [i0, i0+nq) and keys [j0, j0+nk) is
+// visible, so the tile needs no element mask.
+ATTN_HD bool tile_all_visible(int i0, int nq, int j0, int nk, int window) {
+    if (j0 + nk - 1 > i0) return false;                      // some key after some row
+    if (window > 0 && j0 <= i0 + nq - 1 - window) return false;  // some key out of a window
+    return true;
+}
+
 // ---- packed SWA prefill tiling: a tile holds TT = 128/G consecutive query
 // tokens of the G query heads that share one kv head (row r = t*G + hh), and
 // one key tile of N = round_up(TT + W - 1, 16) keys starting at

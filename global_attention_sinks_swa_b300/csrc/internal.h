@@ -68,11 +68,17 @@ int prefill_swa_grid(long max_tiles);
 
 // Backward of the bf16 prefill (D = 128, batches of equal length): dq, dk, dv
 // (bf16) and dsink (fp32), from q, k, v, the forward's o and lse, and dout.
+// The maps view q/dout [B*T, Hq, 128] and k/v [B*T, Hkv, 128] with boxes of
+// (64, 1, rows) for the row counts in their names.
+struct BwdMaps {
+    CUtensorMap q_rows64, dout_rows64, k_rows128, v_rows128;   // dK/dV kernel
+    CUtensorMap q_rows128, dout_rows128, k_rows64, v_rows64;   // dQ kernel
+};
 size_t prefill_backward_workspace(int B, int T, int Hq);
-cudaError_t launch_prefill_backward(const void *q, const void *k, const void *v, const void *o,
-                                    const float *lse, const void *dout, const float *sink,
-                                    void *dq, void *dk, void *dv, float *dsink, void *workspace,
-                                    int B, int T, int Hq, int Hkv, int window, float scale,
+cudaError_t launch_prefill_backward(const BwdMaps &maps, const void *o, const float *lse,
+                                    const void *dout, const float *sink, void *dq, void *dk,
+                                    void *dv, float *dsink, void *workspace, int B, int T, int Hq,
+                                    int Hkv, int window, float scale, unsigned int *err,
                                     cudaStream_t s);
 
 // KV-cache appends (plain 16-byte copies).

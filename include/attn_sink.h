@@ -58,10 +58,11 @@
  *     set bits in a device error word, the offending work is skipped (never a
  *     trap), and attn_check_device_error() reports them;
  *   - while ATTN_DEVERR_WAIT_TIMEOUT is set, the pipelined kernels (the
- *     tensor-core prefill and the verify kernels, the ones with bounded
+ *     tensor-core prefill, verify and backward kernels, the ones with bounded
  *     barrier waits) return without doing any work, so a stalled pipeline is
- *     not run into again; the fp32 prefill, the appends and the backward run
- *     as usual.  attn_check_device_error() clears the word.
+ *     not run into again: their outputs keep their previous contents (the
+ *     backward still writes dsink).  The fp32 prefill and the appends run as
+ *     usual.  attn_check_device_error() clears the word.
  */
 #ifndef ATTN_SINK_H
 #define ATTN_SINK_H
@@ -159,8 +160,10 @@ attn_status_t attn_ga_sink_prefill_varlen(const void *q, const void *k, const vo
  *   window 0 = global attention, else the sliding window; scale as forward.
  * dS_ij = P_ij (<dout_i, v_j> - D_i) with D_i = <dout_i, o_i> and P from the
  * lse; dsink_h = -sum_i p_sink,i D_i.  `workspace` (device, 256-byte
- * aligned, attn_sink_prefill_backward_workspace bytes) holds fp32 dq
- * partials and D. */
+ * aligned, attn_sink_prefill_backward_workspace bytes = 4*B*Hq*T rounded up
+ * to 256) holds D; its contents need no initialisation.  dq, dk and dv are
+ * computed on the tensor cores without atomics, so repeated calls give
+ * identical results. */
 size_t attn_sink_prefill_backward_workspace(int B, int T, int Hq, int D);
 attn_status_t attn_sink_prefill_backward(const void *q, const void *k, const void *v,
                                          const void *o, const float *lse, const void *dout,
