@@ -72,7 +72,9 @@ def test_new_entry_points_reject_null_pointers_on_host():
 
 
 def test_backward_workspace_size():
-    assert A._lib.attn_sink_prefill_backward_workspace(1, 1024, 64, 128) >= 1024 * 64 * 128 * 4 + 64 * 1024 * 4
+    # D = <dO, O> per (b, h, i) in fp32, rounded up to 256 bytes (no dq partials)
+    assert A._lib.attn_sink_prefill_backward_workspace(1, 1024, 64, 128) == 64 * 1024 * 4
+    assert A._lib.attn_sink_prefill_backward_workspace(2, 1000, 3, 128) == (2 * 3 * 1000 * 4 + 255) // 256 * 256
     assert A._lib.attn_sink_prefill_backward_workspace(1, 1024, 64, 64) == 0   # unsupported D
 
 
