@@ -313,19 +313,24 @@ def bench_prefill_packed(A, synth, steps: int, warmup: int, world: int, stream, 
     return ms, flop, nbytes, lens
 
 
-def bench_backward(A, synth, steps: int, warmup: int, world: int, stream, seed: int, T_=T):
-    """SWA backward (dq, dk, dv, dsink), by default at the headline sizes; FLOP
-    = the five products over visible pairs (S, dP, dV, dK, dQ): 10*D*Hq per pair."""
+def bench_backward(A, synth, steps: int, warmup: int, world: int, stream, seed: int, T_=T,
+                   window=W):
+    """Backward (dq, dk, dv, dsink), by default the SWA layer at the headline
+    sizes (window 0: global attention); FLOP = the five products over visible
+    pairs (S, dP, dV, dK, dQ): 10*D*Hq per pair."""
     import torch
     q, k, v, sink = synth.prefill_inputs(B, T_, HQ, HKV, D, seed, device="cuda")
     dout = synth.normal((B, T_, HQ, D), seed + 1, device="cuda")
     lse = torch.empty(B, HQ, T_, device="cuda")
-    o = A.attn_swa_sink_prefill(q, k, v, sink, window=W, lse=lse, stream=stream)
+    if window:
+        o = A.attn_swa_sink_prefill(q, k, v, sink, window=window, lse=lse, stream=stream)
+    else:
+        o = A.attn_ga_sink_prefill(q, k, v, sink, lse=lse, stream=stream)
     ws = torch.empty(A._lib.attn_sink_prefill_backward_workspace(B, T_, HQ, D), dtype=torch.uint8,
                      device="cuda")
 
     def step(_):
-        A.attn_sink_prefill_backward(q, k, v, o, lse, dout, sink, window=W, workspace=ws,
+        A.attn_sink_prefill_backward(q, k, v, o, lse, dout, sink, window=window, workspace=ws,
                                      stream=stream)
 
     with torch.cuda.stream(stream):
@@ -334,7 +339,7 @@ def bench_backward(A, synth, steps: int, warmup: int, world: int, stream, seed: 
         ms = time_region(step, steps, world, stream)
     if A.attn_check_device_error(stream) != 0:
         raise RuntimeError("backward reported a device error")
-    return ms, 10.0 * D * HQ * visible_pairs(T_, W) * B
+    return ms, 10.0 * D * HQ * visible_pairs(T_, window or None) * B
 
 
 def bench_prefill_e2e(A, synth, steps: int, warmup: int, world: int, stream, seed: int):
@@ -618,7 +623,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-parts", action="store_true", help="headline only")
     ap.add_argument("--profile", default="",
-                    help="comma list of swa,ga,verify_ga,verify_ga_fp8,verify_swa,verify_step,backward: run only these kernels "
+                    help="comma list of swa,ga,verify_ga,verify_ga_fp8,verify_swa,verify_step,backward,ga_backward: run only these kernels "
                          "(warmup + steps), no JSON line; for ncu captures")
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -677,6 +682,15 @@ def main():
             "flop": "10*D*Hq per visible pair (five products)",
             "roofline": {"bound": "tensor", "peak": tf_burst, "unit": "TFLOP/s",
                          "frac": flop_bw / (ms_bw * 1e-3) / 1e12 / tf_burst}}
+        ms_gb, flop_gb = bench_backward(A, synth, 3, warmup, world, stream, 1009 + 10 * rank,
+                                        window=0)
+        parts["ga_backward"] = {
+            "config": "B=1 T=32768 Hq=64 Hkv=8 D=128 full causal bf16: dq, dk, dv, dsink",
+            "value": flop_gb / (ms_gb * 1e-3) / 1e12, "unit": "TFLOP/s", "ms": ms_gb,
+            "flop": "10*D*Hq per visible pair (five products)",
+            "roofline": {"bound": "tensor", "peak": tf_burst, "unit": "TFLOP/s",
+                         "frac": flop_gb / (ms_gb * 1e-3) / 1e12 / tf_burst,
+                         "frac_sustained": flop_gb / (ms_gb * 1e-3) / 1e12 / tf_sus}}
         ctx4 = synth.context_lengths(64, 4096, 65536, 1004)
         ms4, kv4 = bench_verify_ga(A, ctx4, np.full(64, QMAX, np.int32), args.steps, warmup, world,
                                    stream, 1004 + 10 * rank)
@@ -773,6 +787,8 @@ def run_profile(A, synth, args, warmup, stream):
             bench_prefill(A, synth, name, args.steps, warmup, 1, stream, 1002)
         elif name == "backward":   # a quarter of the headline length: a small capture
             bench_backward(A, synth, args.steps, warmup, 1, stream, 1008, T_=T // 4)
+        elif name == "ga_backward":
+            bench_backward(A, synth, args.steps, warmup, 1, stream, 1009, T_=T // 4, window=0)
         elif name in ("verify_ga", "verify_ga_fp8"):
             ctx = synth.context_lengths(16, 4096, 65536, 1004)
             bench_verify_ga(A, ctx, np.full(16, QMAX, np.int32), args.steps, warmup, 1, stream, 1004,

@@ -94,3 +94,46 @@ def test_full_size_backward_prefix_rows():
     _close(dq[:, :L], ref[0], "full-size dq prefix")
     _close(dk[:, :L - W], ref[1][:, :L - W], "full-size dk prefix")
     _close(dv[:, :L - W], ref[2][:, :L - W], "full-size dv prefix")
+
+
+def _full_size_run(window, seed):
+    T = 32768
+    q, k, v, sink = synth.prefill_inputs(1, T, 64, 8, 128, seed, device="cuda")
+    dout = synth.normal((1, T, 64, 128), seed + 1, device="cuda")
+    lse = torch.empty(1, 64, T, device="cuda")
+    if window:
+        o = A.attn_swa_sink_prefill(q, k, v, sink, window=window, lse=lse)
+    else:
+        o = A.attn_ga_sink_prefill(q, k, v, sink, lse=lse)
+    dq, dk, dv, _ = A.attn_sink_prefill_backward(q, k, v, o, lse, dout, sink, window=window)
+    assert A.attn_check_device_error() == 0
+    return (q, k, v, sink.cpu().numpy(), dout), (dq, dk, dv)
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_full_size_backward_sampled_rows_and_keys(window):
+    """T = 32768, Hq = 64, Hkv = 8: dq of sampled query rows (each needs only
+    its own softmax) and dk, dv of sampled keys (sums over the rows that see
+    them) against the oracle's row and key gradients.  Under global attention
+    the keys are the last ones, whose rows the oracle can still afford."""
+    T = 32768
+    (q, k, v, sink, dout), (dq, dk, dv) = _full_size_run(window, 1010 + window)
+    rows = np.array([0, 1, 4097, T // 2 + 3, T - 1])
+    got, ref = [], []
+    for h in (0, 37, 63):
+        got.append(dq[0, rows, h].float().cpu().numpy())
+        ref.append(backward.query_row_grads(q, k, v, sink, dout, window or None, 0, h, rows))
+    _close(torch.from_numpy(np.concatenate(got)), np.concatenate(ref), f"dq rows W={window}")
+    # clusters of keys, so the rows that see them stay few
+    clusters = ([np.array([T - 200, T - 77, T - 1])] if not window
+                else [np.array([5, 9]), np.array([16000, 16001, 16100]), np.array([T - 3, T - 1])])
+    gk, gv, rk, rv = [], [], [], []
+    for g in (0, 7):
+        for keys in clusters:
+            a, c = backward.key_row_grads(q, k, v, sink, dout, window or None, 0, g, keys)
+            rk.append(a)
+            rv.append(c)
+            gk.append(dk[0, keys, g].float().cpu().numpy())
+            gv.append(dv[0, keys, g].float().cpu().numpy())
+    _close(torch.from_numpy(np.concatenate(gk)), np.concatenate(rk), f"dk keys W={window}")
+    _close(torch.from_numpy(np.concatenate(gv)), np.concatenate(rv), f"dv keys W={window}")

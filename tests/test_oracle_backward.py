@@ -114,3 +114,26 @@ def test_pins_reject_planted_mistakes(mutant, monkeypatch):
     monkeypatch.setattr(backward, "prefill_backward", bad)
     with pytest.raises(AssertionError):
         test_matches_torch_autograd(1, 9, 4, 2, 8, 3)
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,window,sinks", [
+    (1, 40, 4, 1, 8, None), (2, 33, 4, 2, None, None), (1, 50, 8, 2, 1, None),
+    (1, 37, 2, 1, 100, {0: math.inf, 1: -math.inf}),
+])
+def test_sampled_row_and_key_gradients_equal_the_full_backward(B, T, Hq, Hkv, window, sinks):
+    """query_row_grads / key_row_grads (used for full-size checks, where the
+    full backward is out of reach) give exactly the rows of prefill_backward."""
+    q, k, v, sink, do = _inputs(B, T, Hq, Hkv, 16, seed=T + Hq)
+    for hh, s in (sinks or {}).items():
+        sink[hh] = s
+    dq, dk, dv, _ = backward.prefill_backward(q, k, v, sink, do, window)
+    rows = np.array([0, 1, T // 2, T - 1])
+    keys = np.array([0, 3, T - 5, T - 1])
+    for b in range(B):
+        for h in range(Hq):
+            np.testing.assert_allclose(backward.query_row_grads(q, k, v, sink, do, window, b, h, rows),
+                                       dq[b, rows, h], rtol=1e-10, atol=1e-12)
+        for g in range(Hkv):
+            gk, gv = backward.key_row_grads(q, k, v, sink, do, window, b, g, keys)
+            np.testing.assert_allclose(gk, dk[b, keys, g], rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(gv, dv[b, keys, g], rtol=1e-10, atol=1e-12)
