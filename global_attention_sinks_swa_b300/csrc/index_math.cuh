@@ -109,6 +109,20 @@ ATTN_HD void ga_key_tiles(int q0, int T, int window, int *first, int *last) {
     *first = lo / kTileN;
 }
 
+// Block order of the GA-tiled prefill: block -> (256-row pair, query head,
+// sequence).  The G = Hq/Hkv heads that share a kv head vary fastest, then
+// the pair (latest, i.e. heaviest under causal masking, first), then the kv
+// head, then the sequence: the CTAs resident at one time read one kv head's
+// K/V (16.8 MB at T = 32768, D = 128), which L2 then serves to all of them.
+ATTN_HD void ga_block_coords(int bid, int npairs, int Hq, int Hkv, int *pair, int *h, int *b) {
+    const int G = Hq / Hkv;
+    const int hh = bid % G, rest = bid / G;
+    *pair = npairs - 1 - rest % npairs;
+    const int rest2 = rest / npairs;
+    *h = (rest2 % Hkv) * G + hh;
+    *b = rest2 / Hkv;
+}
+
 // True when some (row, key) pair of the key tile `j` is invisible from the
 // query tile starting at q0, i.e. the tile needs the element mask; interior
 // tiles skip it.

@@ -94,13 +94,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // block -> (pair, head, sequence); heaviest (latest) pairs first for causal
-    // balance.  T bounds every sequence: pairs past a sequence's end exit.
+    // block -> (pair, head, sequence) in ga_block_coords order: one kv head's
+    // query heads together, heaviest (latest) pairs first.  T bounds every
+    // sequence: pairs past a sequence's end exit.
     const int npairs = (T + 255) / 256;
-    const int per = Hq * B;
-    const int pair = npairs - 1 - static_cast<int>(blockIdx.x) / per;
-    const int h = static_cast<int>(blockIdx.x) % Hq;
-    const int b = (static_cast<int>(blockIdx.x) / Hq) % B;
+    int pair, h, b;
+    ga_block_coords(static_cast<int>(blockIdx.x), npairs, Hq, Hkv, &pair, &h, &b);
     const int g = h / (Hq / Hkv);
     const int q0 = pair * 256;
     const SeqSpan span = seq_span(cu, b, T, total);

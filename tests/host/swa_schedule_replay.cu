@@ -59,3 +59,15 @@ extern "C" void ring_visible_host(int32_t *out, int L, int R, int window, int qp
     const RingVisible vis = ring_visible_slots(L, R, window, qpos);
     for (int s = 0; s < R; ++s) out[s] = vis.contains(s) ? ring_slot_position(s, L, R) : -1;
 }
+
+// Block order of the GA-tiled prefill: out[3*bid .. 3*bid+2] = (pair, head, sequence).
+extern "C" void ga_block_coords_host(int32_t *out, int nblocks, int npairs, int Hq, int Hkv) {
+    using namespace attn;
+    for (int bid = 0; bid < nblocks; ++bid) {
+        int pair, h, b;
+        ga_block_coords(bid, npairs, Hq, Hkv, &pair, &h, &b);
+        out[3 * bid] = pair;
+        out[3 * bid + 1] = h;
+        out[3 * bid + 2] = b;
+    }
+}

@@ -5,7 +5,9 @@ functions (index_math.cuh compiled as host code):
   blocks, and never need more live blocks than the ring holds, for batches of
   equal length and for packed batches (cu_seqlens);
 - the ring verify's visible slots (two slot intervals) must be exactly the
-  slots holding positions in the query's window.
+  slots holding positions in the query's window;
+- the GA prefill's block order must cover every (pair, head, sequence) once,
+  with the heads of one kv head adjacent and the heaviest pairs first.
 No GPU needed; the same functions run on the device in test_gpu_index."""
 import ctypes
 import os
@@ -48,6 +50,10 @@ def replay():
                      grid)
         return visits, live
     run.ring_visible = lib.ring_visible_host
+    lib.ga_block_coords_host.argtypes = [np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")] + \
+        [ctypes.c_int] * 4
+    lib.ga_block_coords_host.restype = None
+    run.ga_block_coords = lib.ga_block_coords_host
     return run
 
 
@@ -129,3 +135,28 @@ def test_ring_visible_slots_match_the_definition(replay):
             if max(0, i - W + 1) <= p <= i:
                 exp[p % R] = p
         np.testing.assert_array_equal(got, exp, err_msg=f"L={L} R={R} W={W} i={i}")
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv", [(1, 32768, 64, 8), (2, 300, 4, 1), (3, 1000, 6, 2),
+                                        (1, 256, 8, 8)])
+def test_ga_block_order_is_a_permutation(replay, B, T, Hq, Hkv):
+    """Every (pair, head, sequence) of the GA prefill grid comes from exactly
+    one block; the G heads of one kv head take consecutive blocks of one pair,
+    and within one (kv head, sequence) the pairs run from the last to the first."""
+    npairs = (T + 255) // 256
+    n = npairs * Hq * B
+    out = np.zeros(3 * n, np.int32)
+    replay.ga_block_coords(out, n, npairs, Hq, Hkv)
+    c = out.reshape(n, 3)
+    assert c[:, 0].min() >= 0 and c[:, 0].max() < npairs
+    assert c[:, 1].min() >= 0 and c[:, 1].max() < Hq
+    assert c[:, 2].min() >= 0 and c[:, 2].max() < B
+    keys = (c[:, 2].astype(np.int64) * Hq + c[:, 1]) * npairs + c[:, 0]
+    assert len(np.unique(keys)) == n
+    G = Hq // Hkv
+    groups = c.reshape(n // G, G, 3)
+    assert (groups[:, :, 0] == groups[:, :1, 0]).all()          # one pair per group of blocks
+    assert (groups[:, :, 1] // G == groups[:, :1, 1] // G).all()  # one kv head per group
+    assert (groups[:, :, 1] % G == np.arange(G)).all()
+    pairs = groups[:, 0, 0].reshape(B * Hkv, npairs)
+    assert (pairs == np.arange(npairs - 1, -1, -1)).all()
