@@ -24,8 +24,10 @@
 //                    dK += dS^T Q run with A from TMEM.  dK and dV stay in
 //                    TMEM for the whole CTA;
 //   bwd_dq_kernel    one CTA per (128-row query tile, head, b), the query rows
-//                    on the M side: per step of 64 keys, S = Q K^T and
-//                    dP = dO V^T, dS = P (dP - D) in bf16 in TMEM, then
+//                    on the M side.  The epilogue warps copy the tile's Q and
+//                    dO rows into TMEM, so per step of 64 keys S = Q K^T and
+//                    dP = dO V^T take A from TMEM and read only K and V from
+//                    shared memory; dS = P (dP - D) in bf16 in TMEM, then
 //                    dQ += dS K with A from TMEM.
 // Q, dO, K and V tiles arrive by TMA (128-byte swizzle) through 3-stage rings
 // fed by one producer warp; one thread issues every MMA; S/dP sit in two TMEM
@@ -110,6 +112,27 @@ ATTN_DEV void store_row_bf16(uint32_t taddr, float mul, __nv_bfloat16 *dst, bool
             w.w = ptx::pack_bf16x2(__uint_as_float(r[8 * ch + 6]) * mul, __uint_as_float(r[8 * ch + 7]) * mul);
             if (store) *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * ch) = w;
         }
+    }
+}
+
+// This thread's row of a 128-row bf16 tile held as two 128-byte-swizzled D
+// halves (64 d each) -> 64 TMEM columns at taddr, d pairs in order: the A
+// operand layout of a tcgen05.mma that reads A from TMEM.
+ATTN_DEV void row_to_tmem(const uint8_t *half0, const uint8_t *half1, uint32_t taddr, int row) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {  // 32 d at a time
+        const uint8_t *src = ((q4 >> 1) ? half1 : half0) + row * kHalfRowBytes;
+        uint32_t r[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // logical 16-byte chunk c: d 8c .. 8c+7 of the half
+            const int c = 4 * (q4 & 1) + j;
+            const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ (row & 7)) << 4));
+            r[4 * j + 0] = v.x;
+            r[4 * j + 1] = v.y;
+            r[4 * j + 2] = v.z;
+            r[4 * j + 3] = v.w;
+        }
+        ptx::tmem_st16(taddr + 16 * q4, r);
     }
 }
 
@@ -473,7 +496,7 @@ constexpr int kStages = 3;
 constexpr int kThreads = 512;  // warp 0 TMA, 1 MMA, 4-7 / 8-11 compute, 12-15 epilogue
 constexpr int kQTile = kBQ * kHalfRowBytes;   // 16 KB per D half
 constexpr int kKTile = kBK * kHalfRowBytes;   // 8 KB per D half
-constexpr uint32_t kColDQ = 0, kColBuf = 256;  // dQ slot s at 128s; buffer b: S 256+128b, dP +64
+constexpr uint32_t kColDQ = 0, kColQ = 128, kColDO = 192, kColBuf = 256;  // buffer b: S 256+128b, dP +64
 constexpr uint32_t kIdescS = ptx::idesc_bf16(128, kBK, false, false);
 constexpr uint32_t kIdescAcc = ptx::idesc_bf16(128, 128, false, true);
 
@@ -489,7 +512,7 @@ struct __align__(1024) Smem {
     QBuf qb[2];               // items alternate between two Q/dO buffers
     Stage st[kStages];
     uint64_t q_full[2], q_empty[2], full[kStages], empty[kStages], sdp_full[2], p_full[2];
-    uint64_t dq_full[2], dq_empty[2], mma_done;
+    uint64_t qdo_ready, qdo_used, dq_full, dq_empty, mma_done;
     uint32_t tmem_base;
     int abort;
 };
@@ -524,12 +547,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&sm.q_full[i], 1);
-            ptx::mbar_init(&sm.q_empty[i], 1);
+            ptx::mbar_init(&sm.q_empty[i], 4);  // the epilogue warps, once Q and dO are in TMEM
             ptx::mbar_init(&sm.sdp_full[i], 1);
             ptx::mbar_init(&sm.p_full[i], 4);
-            ptx::mbar_init(&sm.dq_full[i], 1);
-            ptx::mbar_init(&sm.dq_empty[i], 4);
         }
+        ptx::mbar_init(&sm.qdo_ready, 4);
+        ptx::mbar_init(&sm.qdo_used, 1);
+        ptx::mbar_init(&sm.dq_full, 1);
+        ptx::mbar_init(&sm.dq_empty, 4);
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(&sm.full[i], 1);
             ptx::mbar_init(&sm.empty[i], 1);
@@ -601,38 +626,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pn = -1, pk = 0, pt = 0, pN = 0;  // the step whose dQ product is still due
             // dQ += dS K of step n (item k, step t of N), dS in TMEM, K in shared memory
             auto acc_step = [&](int n, int k, int t, int N) {
-                const int s = n % kStages, bb = n & 1, ds = k & 1;
+                const int s = n % kStages, bb = n & 1;
                 if (!ptx::mbar_wait(&sm.p_full[bb], (n >> 1) & 1)) return false;
-                if (t == 0 && k >= 2 && !ptx::mbar_wait(&sm.dq_empty[ds], ((k >> 1) - 1) & 1)) return false;
+                if (t == 0 && k >= 1 && !ptx::mbar_wait(&sm.dq_empty, (k - 1) & 1)) return false;
                 ptx::tc_fence_after();
                 const uint32_t tdS = tmem + kColBuf + 128 * bb + 64;
                 for (int kk = 0; kk < kBK / 16; ++kk)
-                    ptx::mma_ts(tmem + kColDQ + 128 * ds, tdS + kk * 8, vmajor_desc(sm.st[s].k[0], kk, kKTile),
+                    ptx::mma_ts(tmem + kColDQ, tdS + kk * 8, vmajor_desc(sm.st[s].k[0], kk, kKTile),
                                 kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
                 ptx::tc_commit(&sm.empty[s]);
-                if (t == N - 1) ptx::tc_commit(&sm.dq_full[ds]);
+                if (t == N - 1) ptx::tc_commit(&sm.dq_full);
                 return true;
             };
             int n = 0, k = 0;
             for (int it = cta; ok && it < pr.nitems; it += grid, ++k) {
                 int i0, h, b, kt0, nkt;
                 pr.item(it, i0, h, b, kt0, nkt);
-                const int qs = k & 1;
-                if (!(ok = !aborted() && ptx::mbar_wait(&sm.q_full[qs], (k >> 1) & 1))) break;
+                // this item's Q and dO rows are in TMEM (copied by the epilogue warps)
+                if (!(ok = !aborted() && ptx::mbar_wait(&sm.qdo_ready, k & 1))) break;
                 for (int t = 0; t < nkt; ++t, ++n) {
-                    // S = Q K^T and dP = dO V^T into buffer n mod 2
+                    // S = Q K^T and dP = dO V^T into buffer n mod 2, A from TMEM
                     const int s = n % kStages, bb = n & 1;
                     if (!(ok = ptx::mbar_wait(&sm.full[s], (n / kStages) & 1))) break;
                     ptx::tc_fence_after();
                     const uint32_t tS = tmem + kColBuf + 128 * bb, tdP = tS + 64;
                     for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_ss(tS, kmajor_desc(sm.qb[qs].q[kk >> 2], kk & 3),
-                                    kmajor_desc(sm.st[s].k[kk >> 2], kk & 3), kIdescS, kk > 0);
+                        ptx::mma_ts(tS, tmem + kColQ + kk * 8, kmajor_desc(sm.st[s].k[kk >> 2], kk & 3),
+                                    kIdescS, kk > 0);
                     for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_ss(tdP, kmajor_desc(sm.qb[qs].dout[kk >> 2], kk & 3),
-                                    kmajor_desc(sm.st[s].v[kk >> 2], kk & 3), kIdescS, kk > 0);
+                        ptx::mma_ts(tdP, tmem + kColDO + kk * 8, kmajor_desc(sm.st[s].v[kk >> 2], kk & 3),
+                                    kIdescS, kk > 0);
                     ptx::tc_commit(&sm.sdp_full[bb]);
-                    if (t == nkt - 1) ptx::tc_commit(&sm.q_empty[qs]);
+                    if (t == nkt - 1) ptx::tc_commit(&sm.qdo_used);  // TMEM Q/dO free once these complete
                     issued = true;
                     if (pn >= 0 && !(ok = acc_step(pn, pk, pt, pN))) break;
                     pn = n;
@@ -681,25 +706,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok && lane == 0) fail();
     } else if (warp >= 12 && !skip) {
-        // ------------------------------- epilogue: dQ (x scale) of each item -> bf16
+        // ---- epilogue: each item's Q and dO rows into TMEM, then the previous
+        // item's dQ (x scale) -> bf16
         const int row = threadIdx.x & 127;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        int k = 0;
+        auto drain = [&](int k, int i0, int h, int b) {  // dQ of item k
+            if (__any_sync(0xffffffffu, aborted()) || !ptx::mbar_wait_warp(&sm.dq_full, k & 1))
+                return false;
+            ptx::tc_fence_after();
+            const int i = i0 + row;
+            store_row_bf16<128>(tmem + lane_off + kColDQ, scale,
+                                dq + ((static_cast<long>(b) * T + (i < T ? i : 0)) * Hq + h) * kD, i < T);
+            ptx::tc_fence_before();
+            if (lane == 0) ptx::mbar_arrive(&sm.dq_empty);
+            return true;
+        };
+        bool ok = true;
+        int k = 0, pi0 = 0, ph = 0, pb = 0;  // the previous item
         for (int it = cta; it < pr.nitems; it += grid, ++k) {
             int i0, h, b, kt0, nkt;
             pr.item(it, i0, h, b, kt0, nkt);
-            const int ds = k & 1;
-            if (__any_sync(0xffffffffu, aborted()) || !ptx::mbar_wait_warp(&sm.dq_full[ds], (k >> 1) & 1)) {
-                if (lane == 0) fail();
+            const int qs = k & 1;
+            // the tile's Q and dO have landed, and the previous item's
+            // products no longer read the TMEM copies
+            if (__any_sync(0xffffffffu, aborted()) || !ptx::mbar_wait_warp(&sm.q_full[qs], (k >> 1) & 1) ||
+                (k >= 1 && !ptx::mbar_wait_warp(&sm.qdo_used, (k - 1) & 1))) {
+                ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const int i = i0 + row;
-            store_row_bf16<128>(tmem + lane_off + kColDQ + 128 * ds, scale,
-                                dq + ((static_cast<long>(b) * T + (i < T ? i : 0)) * Hq + h) * kD, i < T);
+            row_to_tmem(sm.qb[qs].q[0], sm.qb[qs].q[1], tmem + lane_off + kColQ, row);
+            row_to_tmem(sm.qb[qs].dout[0], sm.qb[qs].dout[1], tmem + lane_off + kColDO, row);
+            ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            if (lane == 0) ptx::mbar_arrive(&sm.dq_empty[ds]);
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(&sm.qdo_ready);
+                ptx::mbar_arrive(&sm.q_empty[qs]);  // the shared-memory tile may take item k + 2
+            }
+            if (k >= 1 && !(ok = drain(k - 1, pi0, ph, pb))) break;
+            pi0 = i0;
+            ph = h;
+            pb = b;
         }
+        if (ok && k >= 1) ok = drain(k - 1, pi0, ph, pb);
+        if (!ok && lane == 0) fail();
     }
     __syncwarp();
     ptx::tc_fence_before();
