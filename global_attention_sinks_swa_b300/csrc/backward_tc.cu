@@ -115,27 +115,6 @@ ATTN_DEV void store_row_bf16(uint32_t taddr, float mul, __nv_bfloat16 *dst, bool
     }
 }
 
-// This thread's row of a 128-row bf16 tile held as two 128-byte-swizzled D
-// halves (64 d each) -> 64 TMEM columns at taddr, d pairs in order: the A
-// operand layout of a tcgen05.mma that reads A from TMEM.
-ATTN_DEV void row_to_tmem(const uint8_t *half0, const uint8_t *half1, uint32_t taddr, int row) {
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {  // 32 d at a time
-        const uint8_t *src = ((q4 >> 1) ? half1 : half0) + row * kHalfRowBytes;
-        uint32_t r[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {  // logical 16-byte chunk c: d 8c .. 8c+7 of the half
-            const int c = 4 * (q4 & 1) + j;
-            const uint4 v = *reinterpret_cast<const uint4 *>(src + ((c ^ (row & 7)) << 4));
-            r[4 * j + 0] = v.x;
-            r[4 * j + 1] = v.y;
-            r[4 * j + 2] = v.z;
-            r[4 * j + 3] = v.w;
-        }
-        ptx::tmem_st16(taddr + 16 * q4, r);
-    }
-}
-
 // Four consecutive fp32 values from shared memory (16-byte aligned).
 ATTN_DEV float4 lds4(const float *p) {
     float4 v;
