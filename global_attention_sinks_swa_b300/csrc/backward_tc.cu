@@ -127,12 +127,15 @@ ATTN_DEV float4 lds4(const float *p) {
 // One compute step of 64 columns (queries for dK/dV, keys for dQ) of this
 // thread's TMEM lane: P = 2^(S*scale*log2e - lse2) on the visible columns
 // [lo, hi) and 0 elsewhere, dS = P (dP - delta); P (if wanted) replaces S and
-// dS replaces dP as packed bf16 (32 columns each).  lse2/delta are per column
-// (arrays in shared memory, kColumns) or one value for the row.  The mask is
-// a select after the exponential, never a branch.
+// dS replaces dP as packed bf16 (32 columns each).  The negated lse2 and
+// delta come per column (arrays in shared memory, kColumns) or as one value
+// for the row.  The mask is a select after the exponential, never a branch;
+// the fp32 arithmetic runs on pairs (f32x2), half the FMA-pipe instructions.
 template <bool kWantP, bool kColumns>
-ATTN_DEV void p_ds_step(uint32_t tS, uint32_t tdP, float sl2, const float *lse2_col,
-                        const float *delta_col, float lse2_row, float delta_row, int lo, int hi) {
+ATTN_DEV void p_ds_step(uint32_t tS, uint32_t tdP, float sl2, const float *nlse2_col,
+                        const float *ndelta_col, float nlse2_row, float ndelta_row, int lo, int hi) {
+    const uint64_t sl2x2 = f2(sl2, sl2);
+    const uint64_t nl_row = f2(nlse2_row, nlse2_row), nd_row = f2(ndelta_row, ndelta_row);
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t pk[16], dk[16];
@@ -147,31 +150,36 @@ ATTN_DEV void p_ds_step(uint32_t tS, uint32_t tdP, float sl2, const float *lse2_
             reg_dep(dp);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                float l4[4], d4[4];
+                uint64_t nl01 = nl_row, nl23 = nl_row, nd01 = nd_row, nd23 = nd_row;
                 if constexpr (kColumns) {
-                    const float4 lv = lds4(lse2_col + cb + 4 * q);
-                    const float4 dv = lds4(delta_col + cb + 4 * q);
-                    l4[0] = lv.x; l4[1] = lv.y; l4[2] = lv.z; l4[3] = lv.w;
-                    d4[0] = dv.x; d4[1] = dv.y; d4[2] = dv.z; d4[3] = dv.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        l4[e] = lse2_row;
-                        d4[e] = delta_row;
-                    }
+                    const float4 lv = lds4(nlse2_col + cb + 4 * q);
+                    const float4 dv = lds4(ndelta_col + cb + 4 * q);
+                    nl01 = f2(lv.x, lv.y);
+                    nl23 = f2(lv.z, lv.w);
+                    nd01 = f2(dv.x, dv.y);
+                    nd23 = f2(dv.z, dv.w);
                 }
-                float p[4], d[4];
+                const float2 a01 = f2_split(f2_fma(
+                    f2(__uint_as_float(s[4 * q]), __uint_as_float(s[4 * q + 1])), sl2x2, nl01));
+                const float2 a23 = f2_split(f2_fma(
+                    f2(__uint_as_float(s[4 * q + 2]), __uint_as_float(s[4 * q + 3])), sl2x2, nl23));
+                float p[4] = {ptx::exp2_approx(a01.x), ptx::exp2_approx(a01.y),
+                              ptx::exp2_approx(a23.x), ptx::exp2_approx(a23.y)};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = cb + 4 * q + e;
-                    const float x = ptx::exp2_approx(fmaf(__uint_as_float(s[4 * q + e]), sl2, -l4[e]));
-                    p[e] = (c >= lo && c < hi) ? x : 0.f;
-                    d[e] = p[e] * (__uint_as_float(dp[4 * q + e]) - d4[e]);
+                    p[e] = (c >= lo && c < hi) ? p[e] : 0.f;
                 }
+                const float2 d01 = f2_split(f2_mul(
+                    f2(p[0], p[1]),
+                    f2_add(f2(__uint_as_float(dp[4 * q]), __uint_as_float(dp[4 * q + 1])), nd01)));
+                const float2 d23 = f2_split(f2_mul(
+                    f2(p[2], p[3]),
+                    f2_add(f2(__uint_as_float(dp[4 * q + 2]), __uint_as_float(dp[4 * q + 3])), nd23)));
                 pk[8 * c4 + 2 * q] = ptx::pack_bf16x2(p[0], p[1]);
                 pk[8 * c4 + 2 * q + 1] = ptx::pack_bf16x2(p[2], p[3]);
-                dk[8 * c4 + 2 * q] = ptx::pack_bf16x2(d[0], d[1]);
-                dk[8 * c4 + 2 * q + 1] = ptx::pack_bf16x2(d[2], d[3]);
+                dk[8 * c4 + 2 * q] = ptx::pack_bf16x2(d01.x, d01.y);
+                dk[8 * c4 + 2 * q + 1] = ptx::pack_bf16x2(d23.x, d23.y);
             }
         }
         if constexpr (kWantP) ptx::tmem_st16(tS + 16 * c2, pk);
@@ -214,8 +222,8 @@ constexpr uint32_t kIdescAcc = ptx::idesc_bf16(128, 128, false, true);
 struct __align__(1024) Stage {
     uint8_t q[2][kQTile];     // [D half][row][64]
     uint8_t dout[2][kQTile];
-    float lse2[kBQ];          // lse * log2(e); +inf for rows past T (so P = 0 there)
-    float delta[kBQ];
+    float nlse2[kBQ];         // -lse * log2(e); -inf for rows past T (so P = 0 there)
+    float ndelta[kBQ];        // -D
 };
 struct __align__(1024) Smem {
     uint8_t k[2][kKTile];
@@ -315,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int i = i0 + lane + 32 * e;
-                    l2[e] = i < T ? lse[base + i] * kLog2e : INFINITY;
-                    dl[e] = i < T ? delta[base + i] : 0.f;
+                    l2[e] = i < T ? -lse[base + i] * kLog2e : -INFINITY;
+                    dl[e] = i < T ? -delta[base + i] : 0.f;
                 }
                 const int s = n % kStages;
                 if (n >= kStages && (aborted() || !(ok = ptx::mbar_wait_warp(&sm.empty[s], ((n / kStages) - 1) & 1)))) {
@@ -325,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    sm.st[s].lse2[lane + 32 * e] = l2[e];
-                    sm.st[s].delta[lane + 32 * e] = dl[e];
+                    sm.st[s].nlse2[lane + 32 * e] = l2[e];
+                    sm.st[s].ndelta[lane + 32 * e] = dl[e];
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -428,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Stage &st = sm.st[n % kStages];
                 int lo, hi;
                 cols_for_key(key, i0, window, lo, hi);
-                p_ds_step<true, true>(tS, tdP, sl2, st.lse2, st.delta, 0.f, 0.f, lo, hi);
+                p_ds_step<true, true>(tS, tdP, sl2, st.nlse2, st.ndelta, 0.f, 0.f, lo, hi);
                 ptx::tc_fence_before();
                 if (lane == 0) ptx::mbar_arrive(&sm.p_full[j]);
             }
@@ -667,8 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = i0 + row;
             // this row's lse and D, read while the first step's products run
             const long li = (static_cast<long>(b) * Hq + h) * T + (i < T ? i : 0);
-            const float lse2 = i < T ? lse[li] * kLog2e : INFINITY;  // rows past T: P = 0
-            const float dlt = i < T ? delta[li] : 0.f;
+            const float nlse2 = i < T ? -lse[li] * kLog2e : -INFINITY;  // rows past T: P = 0
+            const float ndlt = i < T ? -delta[li] : 0.f;
             for (int t = 0; t < nkt; ++t, ++n) {
                 if ((n & 1) != j) continue;
                 if (!(ok = !__any_sync(0xffffffffu, aborted()) &&
@@ -678,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j0 = (kt0 + t) * kBK;
                 int lo, hi;
                 cols_for_query(i, j0, window, lo, hi);
-                p_ds_step<false, false>(tS, tdP, sl2, nullptr, nullptr, lse2, dlt, lo, hi);
+                p_ds_step<false, false>(tS, tdP, sl2, nullptr, nullptr, nlse2, ndlt, lo, hi);
                 ptx::tc_fence_before();
                 if (lane == 0) ptx::mbar_arrive(&sm.p_full[j]);
             }
