@@ -129,9 +129,10 @@ ATTN_DEV float4 lds4(const float *p) {
 // [lo, hi) and 0 elsewhere, dS = P (dP - delta); P (if wanted) replaces S and
 // dS replaces dP as packed bf16 (32 columns each).  The negated lse2 and
 // delta come per column (arrays in shared memory, kColumns) or as one value
-// for the row.  The mask is a select after the exponential, never a branch;
-// the fp32 arithmetic runs on pairs (f32x2), half the FMA-pipe instructions.
-template <bool kWantP, bool kColumns>
+// for the row.  The mask (kMask; without it every column is visible) is a
+// select after the exponential, never a branch; the fp32 arithmetic runs on
+// pairs (f32x2), half the FMA-pipe instructions.
+template <bool kWantP, bool kColumns, bool kMask>
 ATTN_DEV void p_ds_step(uint32_t tS, uint32_t tdP, float sl2, const float *nlse2_col,
                         const float *ndelta_col, float nlse2_row, float ndelta_row, int lo, int hi) {
     const uint64_t sl2x2 = f2(sl2, sl2);
@@ -165,10 +166,12 @@ ATTN_DEV void p_ds_step(uint32_t tS, uint32_t tdP, float sl2, const float *nlse2
                     f2(__uint_as_float(s[4 * q + 2]), __uint_as_float(s[4 * q + 3])), sl2x2, nl23));
                 float p[4] = {ptx::exp2_approx(a01.x), ptx::exp2_approx(a01.y),
                               ptx::exp2_approx(a23.x), ptx::exp2_approx(a23.y)};
+                if constexpr (kMask) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = cb + 4 * q + e;
-                    p[e] = (c >= lo && c < hi) ? p[e] : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = cb + 4 * q + e;
+                        p[e] = (c >= lo && c < hi) ? p[e] : 0.f;
+                    }
                 }
                 const float2 d01 = f2_split(f2_mul(
                     f2(p[0], p[1]),
@@ -436,7 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Stage &st = sm.st[n % kStages];
                 int lo, hi;
                 cols_for_key(key, i0, window, lo, hi);
-                p_ds_step<true, true>(tS, tdP, sl2, st.nlse2, st.ndelta, 0.f, 0.f, lo, hi);
+                // a step whose 64 columns this warp's rows all see skips the mask
+                if (__all_sync(0xffffffffu, lo <= 0 && hi >= kBQ))
+                    p_ds_step<true, true, false>(tS, tdP, sl2, st.nlse2, st.ndelta, 0.f, 0.f, lo, hi);
+                else
+                    p_ds_step<true, true, true>(tS, tdP, sl2, st.nlse2, st.ndelta, 0.f, 0.f, lo, hi);
                 ptx::tc_fence_before();
                 if (lane == 0) ptx::mbar_arrive(&sm.p_full[j]);
             }
@@ -686,7 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j0 = (kt0 + t) * kBK;
                 int lo, hi;
                 cols_for_query(i, j0, window, lo, hi);
-                p_ds_step<false, false>(tS, tdP, sl2, nullptr, nullptr, nlse2, ndlt, lo, hi);
+                if (__all_sync(0xffffffffu, lo <= 0 && hi >= kBK))
+                    p_ds_step<false, false, false>(tS, tdP, sl2, nullptr, nullptr, nlse2, ndlt, lo, hi);
+                else
+                    p_ds_step<false, false, true>(tS, tdP, sl2, nullptr, nullptr, nlse2, ndlt, lo, hi);
                 ptx::tc_fence_before();
                 if (lane == 0) ptx::mbar_arrive(&sm.p_full[j]);
             }
