@@ -255,21 +255,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
             m = mn;
             const float mb = (m == -INFINITY) ? 0.f : m;
-            float r4[4] = {0.f, 0.f, 0.f, 0.f};
+            // P = 2^(s*scale*log2e - m) as bf16 over the S columns; paired fp32
+            // arithmetic, partial sums of the columns j mod 4 (l2[j>>1], half j&1)
+            const uint64_t sl2x2 = f2(sl2, sl2), nmb = f2(-mb, -mb);
+            uint64_t l2[2] = {0, 0};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {  // P = 2^(s*scale*log2e - m) as bf16 over the S columns
+            for (int c = 0; c < 4; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ptx::exp2_approx(fmaf(x[32 * c + 2 * i], sl2, -mb));
-                    const float p1 = ptx::exp2_approx(fmaf(x[32 * c + 2 * i + 1], sl2, -mb));
-                    r4[(2 * i) & 3] += p0;
-                    r4[(2 * i + 1) & 3] += p1;
+                    const float2 a = f2_split(f2_fma(f2(x[32 * c + 2 * i], x[32 * c + 2 * i + 1]), sl2x2, nmb));
+                    const float p0 = ptx::exp2_approx(a.x), p1 = ptx::exp2_approx(a.y);
+                    l2[i & 1] = f2_add(l2[i & 1], f2(p0, p1));
                     pk[i] = ptx::pack_bf16x2(p0, p1);
                 }
                 ptx::tmem_st16(tS + 16 * c, pk);
             }
-            l += (r4[0] + r4[1]) + (r4[2] + r4[3]);
+            const float2 la = f2_split(l2[0]), lb = f2_split(l2[1]);
+            l += (la.x + la.y) + (lb.x + lb.y);
             if (any_grow && nt > 0) {  // rescale the O accumulator after the previous PV
                 if (!ptx::mbar_wait_warp(&sm.o_full[t], (nt - 1) & 1)) { ok = false; break; }
                 ptx::tc_fence_after();
