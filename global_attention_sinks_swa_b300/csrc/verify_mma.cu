@@ -15,7 +15,8 @@
 // 128-byte-swizzled shared-memory tiles.  Warp roles: warp 4 issues the TMA
 // loads; warps 0-3 compute, warp w owning rows [16(w&1), +16) and keys
 // [32(w>>1), +32) of every block, with mma.sync m16n8k16 for S = QK^T and
-// O += PV and an online softmax in registers.  The two key halves merge in
+// O += PV and an online softmax in registers (its running max raised only
+// when a block exceeds it by more than 2^8).  The two key halves merge in
 // shared memory; the sink logit joins the denominator once, in the final
 // merge (in-kernel for the ring, in the split combine for the paged cache).
 //
@@ -48,6 +49,7 @@ constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kHalfBytes = kVerifyBlock * 128;  // 64 rows x 128 B (64 bf16)
 constexpr int kStageBytes = 4 * kHalfBytes;      // K and V, two D halves each
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
 constexpr unsigned kErrPage = 0x1u, kErrCtx = 0x2u, kErrQlen = 0x4u, kErrWait = 0x8u;
 constexpr int kMergeStride = kD + 8;     // floats per row of the key-half merge buffer
 constexpr int kStageRowBytes = 2 * kD + 16;  // bytes per row of the bf16 output staging
@@ -390,17 +392,33 @@ __global__ void __launch_bounds__(kThreads, 2)
                         mx[e >> 1] = fmaxf(mx[e >> 1], val);
                     }
             }
-            float alpha[2], mbase[2];
+            // the running max is raised lazily: only when a row's block max
+            // exceeds it by more than 2^8, so O is rarely rescaled and every
+            // weight stays <= 2^8 (well inside bf16 / f16)
+            bool grow = false;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 mx[h2] = fmaxf(mx[h2], __shfl_xor_sync(0xffffffffu, mx[h2], 1));
                 mx[h2] = fmaxf(mx[h2], __shfl_xor_sync(0xffffffffu, mx[h2], 2));
-                const float mn = fmaxf(mrow[h2], mx[h2]);
-                mbase[h2] = (mn == -INFINITY) ? 0.f : mn;
-                alpha[h2] = ptx::exp2_approx(mrow[h2] - mbase[h2]);
-                mrow[h2] = mn;
-                lrow[h2] *= alpha[h2];
+                grow |= mx[h2] > mrow[h2] + kRescaleLog2;
             }
+            if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const float mn = fmaxf(mrow[h2], mx[h2]);
+                    const float alpha = ptx::exp2_approx(mrow[h2] - (mn == -INFINITY ? 0.f : mn));
+                    mrow[h2] = mn;
+                    lrow[h2] *= alpha;
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        oacc[n][2 * h2] *= alpha;
+                        oacc[n][2 * h2 + 1] *= alpha;
+                    }
+                }
+            }
+            float mbase[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) mbase[h2] = (mrow[h2] == -INFINITY) ? 0.f : mrow[h2];
 #pragma unroll
             for (int n = 0; n < 4; ++n)
 #pragma unroll
@@ -409,13 +427,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                     s[n][e] = pv;
                     lrow[e >> 1] += pv;
                 }
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                oacc[n][0] *= alpha[0];
-                oacc[n][1] *= alpha[0];
-                oacc[n][2] *= alpha[1];
-                oacc[n][3] *= alpha[1];
-            }
             // O += P V  (P from registers as bf16 A fragments)
 #pragma unroll
             for (int k2 = 0; k2 < 2; ++k2) {
