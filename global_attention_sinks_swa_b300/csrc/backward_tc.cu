@@ -115,6 +115,13 @@ ATTN_DEV void store_row_bf16(uint32_t taddr, float mul, __nv_bfloat16 *dst, bool
     }
 }
 
+// Eight consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
+ATTN_DEV void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 ATTN_I8(0)
+                 : "memory");
+}
+
 // Four consecutive fp32 values from shared memory (16-byte aligned).
 ATTN_DEV float4 lds4(const float *p) {
     float4 v;
@@ -139,10 +146,10 @@ ATTN_DEV void p_ds_step(uint32_t tS, uint32_t tdP, float sl2, const float *nlse2
     const uint64_t nl_row = f2(nlse2_row, nlse2_row), nd_row = f2(ndelta_row, ndelta_row);
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t pk[16], dk[16];
 #pragma unroll
         for (int c4 = 0; c4 < 2; ++c4) {  // 16 columns at a time
             const int cb = 32 * c2 + 16 * c4;
+            uint32_t pk[8], dk[8];
             uint32_t s[16], dp[16];
             ptx::tmem_ld16(tS + cb, s);
             ptx::tmem_ld16(tdP + cb, dp);
@@ -179,14 +186,14 @@ ATTN_DEV void p_ds_step(uint32_t tS, uint32_t tdP, float sl2, const float *nlse2
                 const float2 d23 = f2_split(f2_mul(
                     f2(p[2], p[3]),
                     f2_add(f2(__uint_as_float(dp[4 * q + 2]), __uint_as_float(dp[4 * q + 3])), nd23)));
-                pk[8 * c4 + 2 * q] = ptx::pack_bf16x2(p[0], p[1]);
-                pk[8 * c4 + 2 * q + 1] = ptx::pack_bf16x2(p[2], p[3]);
-                dk[8 * c4 + 2 * q] = ptx::pack_bf16x2(d01.x, d01.y);
-                dk[8 * c4 + 2 * q + 1] = ptx::pack_bf16x2(d23.x, d23.y);
+                pk[2 * q] = ptx::pack_bf16x2(p[0], p[1]);
+                pk[2 * q + 1] = ptx::pack_bf16x2(p[2], p[3]);
+                dk[2 * q] = ptx::pack_bf16x2(d01.x, d01.y);
+                dk[2 * q + 1] = ptx::pack_bf16x2(d23.x, d23.y);
             }
+            if constexpr (kWantP) tmem_st8(tS + cb / 2, pk);
+            tmem_st8(tdP + cb / 2, dk);
         }
-        if constexpr (kWantP) ptx::tmem_st16(tS + 16 * c2, pk);
-        ptx::tmem_st16(tdP + 16 * c2, dk);
     }
     ptx::tmem_st_wait();
 }
