@@ -115,12 +115,17 @@ attn_status_t attn_check_device_error(void *stream, unsigned int *bits_out);
  * Supported: ATTN_BF16 with D = 128 and 128 % (Hq/Hkv) == 0 on the tensor cores
  * (Hq/Hkv = 8 with window in [114, 129] on the streaming kernel, any other
  * ratio or window on the GA-tiled kernel with window-limited tile skipping);
- * ATTN_F32 with D in {64,128} on the fp32 CUDA-core path. */
+ * ATTN_F32 with D in {64,128} on the fp32 CUDA-core path.
+ * While ATTN_DEVERR_WAIT_TIMEOUT is set (conventions above) the bf16
+ * tensor-core kernels of this call return at once and o / lse keep their
+ * previous contents: a caller that never polls attn_check_device_error()
+ * cannot tell, so poll after each step or batch of steps. */
 attn_status_t attn_swa_sink_prefill(const void *q, const void *k, const void *v, const float *sink,
                                     void *o, float *lse, int B, int T, int Hq, int Hkv, int D,
                                     int window, float scale, attn_dtype_t dtype, void *stream);
 
-/* Global (full causal) prefill [ARCH][SINK]; arguments as above without window. */
+/* Global (full causal) prefill [ARCH][SINK]; arguments, kernel support and the
+ * behaviour under ATTN_DEVERR_WAIT_TIMEOUT as above, without window. */
 attn_status_t attn_ga_sink_prefill(const void *q, const void *k, const void *v, const float *sink,
                                    void *o, float *lse, int B, int T, int Hq, int Hkv, int D,
                                    float scale, attn_dtype_t dtype, void *stream);
@@ -137,7 +142,8 @@ attn_status_t attn_ga_sink_prefill(const void *q, const void *k, const void *v, 
  * A span that is decreasing, outside [0, total_tokens) or longer than
  * max_seqlen is skipped (its rows are not written) and sets
  * ATTN_DEVERR_SEQLENS.  Everything else as in the calls above (same dtype,
- * D and kernel support; the sliding-window form keeps window >= 1). */
+ * D and kernel support; the sliding-window form keeps window >= 1; while
+ * ATTN_DEVERR_WAIT_TIMEOUT is set the bf16 kernels write nothing). */
 attn_status_t attn_swa_sink_prefill_varlen(const void *q, const void *k, const void *v,
                                            const int32_t *cu_seqlens, const float *sink, void *o,
                                            float *lse, int B, int total_tokens, int max_seqlen,
@@ -163,7 +169,9 @@ attn_status_t attn_ga_sink_prefill_varlen(const void *q, const void *k, const vo
  * aligned, attn_sink_prefill_backward_workspace bytes = 4*B*Hq*T rounded up
  * to 256) holds D; its contents need no initialisation.  dq, dk and dv are
  * computed on the tensor cores without atomics, so repeated calls give
- * identical results. */
+ * identical results.  While ATTN_DEVERR_WAIT_TIMEOUT is set only dsink is
+ * written (dq, dk, dv keep their previous contents): poll
+ * attn_check_device_error(). */
 size_t attn_sink_prefill_backward_workspace(int B, int T, int Hq, int D);
 attn_status_t attn_sink_prefill_backward(const void *q, const void *k, const void *v,
                                          const void *o, const float *lse, const void *dout,
@@ -215,7 +223,9 @@ attn_status_t attn_ga_paged_append_fp8(const void *k_new, const void *v_new,
  *   q, o [cu_q[B],Hq,D] (dtype);  sink [Hq] fp32;  q_max <= 4.
  * Rejected drafts are rolled back by the caller lowering seq_lens; the next
  * append overwrites their slots.  Supported: ATTN_BF16, D = 128,
- * q_max * (Hq/Hkv) <= 32. */
+ * q_max * (Hq/Hkv) <= 32.  While ATTN_DEVERR_WAIT_TIMEOUT is set the verify
+ * kernels (and the split-KV merge) write nothing and o keeps its previous
+ * contents: poll attn_check_device_error() after each step. */
 attn_status_t attn_swa_sink_verify(const void *q, const int32_t *cu_q, const void *ring_k,
                                    const void *ring_v, const int32_t *seq_lens, const float *sink,
                                    void *o, int B, int Hq, int Hkv, int D, int window,
