@@ -58,6 +58,9 @@ def _run(B, T, Hq, Hkv, window, seed, sink_override=None):
 @pytest.mark.parametrize("B,T,Hq,Hkv,window", [
     (1, 200, 16, 2, 128), (2, 77, 8, 1, 64), (1, 300, 8, 8, 0), (1, 1, 8, 2, 128),
     (1, 129, 64, 8, 128), (1, 513, 8, 1, 128),
+    # more query-tile items than CTAs: each persistent CTA reuses its TMEM Q/dO
+    # copy and its dQ accumulator across items
+    (1, 1100, 32, 4, 128), (1, 700, 32, 4, 0),
 ])
 def test_backward_matches_oracle(B, T, Hq, Hkv, window):
     got, ref = _run(B, T, Hq, Hkv, window, seed=T + Hq)
