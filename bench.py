@@ -97,11 +97,62 @@ def ncu_traffic(kernel_file: str, name: str):
     return None
 
 
+class CtypesNvml:
+    """The few read-only NVML queries the clock sampler needs, called through
+    ctypes on the driver's libnvidia-ml (for hosts without the `pynvml`
+    module).  Same names and constants as pynvml's; `lib` may be any object
+    with the NVML C entry points (tests pass a fake)."""
+
+    NVML_CLOCK_SM = 1
+    # clock event reason bits of the NVML API
+    nvmlClocksEventReasonSwPowerCap = 0x4
+    nvmlClocksEventReasonHwSlowdown = 0x8
+    nvmlClocksEventReasonSwThermalSlowdown = 0x20
+    nvmlClocksEventReasonHwThermalSlowdown = 0x40
+
+    def __init__(self, lib=None):
+        import ctypes
+        self._c = ctypes
+        self._lib = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+
+    def _ok(self, rc, what):
+        if rc != 0:
+            raise RuntimeError(f"{what} returned {rc}")
+
+    def nvmlInit(self):
+        self._ok(self._lib.nvmlInit_v2(), "nvmlInit_v2")
+
+    def nvmlDeviceGetHandleByIndex(self, index):
+        h = self._c.c_void_p()
+        self._ok(self._lib.nvmlDeviceGetHandleByIndex_v2(self._c.c_uint(index), self._c.byref(h)),
+                 "nvmlDeviceGetHandleByIndex_v2")
+        return h
+
+    def _clock(self, fn, handle, kind):
+        v = self._c.c_uint()
+        self._ok(getattr(self._lib, fn)(handle, self._c.c_int(kind), self._c.byref(v)), fn)
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, handle, kind):
+        return self._clock("nvmlDeviceGetClockInfo", handle, kind)
+
+    def nvmlDeviceGetMaxClockInfo(self, handle, kind):
+        return self._clock("nvmlDeviceGetMaxClockInfo", handle, kind)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, handle):
+        v = self._c.c_ulonglong()
+        fn = getattr(self._lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._ok(fn(handle, self._c.byref(v)), "nvmlDeviceGetCurrentClocksEventReasons")
+        return v.value
+
+
 class ClockSampler:
     """SM clock and throttle reasons sampled during a timed region (read-only
-    queries).  NVML is polled every ~2 ms in a thread when the `pynvml`
-    module is present; otherwise `nvidia-smi -lms 20` runs for the region and
-    the sampler waits for its first line before the region starts."""
+    queries).  NVML is polled every ~2 ms in a thread, through the `pynvml`
+    module or, without it, through ctypes on the driver's NVML library;
+    failing both, `nvidia-smi -lms 20` runs for the region and the sampler
+    waits for its first line before the region starts."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -152,19 +203,28 @@ class ClockSampler:
                                        if v.lower() == "active"}))
             self._first.set()
 
+    def _start_nvml(self, nvml, source):
+        nvml.nvmlInit()
+        self._nvml = nvml
+        self._h = nvml.nvmlDeviceGetHandleByIndex(self.gpu)
+        self.sm_max = float(nvml.nvmlDeviceGetMaxClockInfo(self._h, nvml.NVML_CLOCK_SM))
+        self.source = source
+        self._thread = threading.Thread(target=self._nvml_poll, daemon=True)
+        self._thread.start()
+
     def __enter__(self):
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nvml = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.gpu)
-            self.sm_max = float(pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM))
-            self.source = "nvml"
-            self._thread = threading.Thread(target=self._nvml_poll, daemon=True)
-            self._thread.start()
-            return self
-        except Exception as e:  # noqa: BLE001
-            self.error = f"nvml: {type(e).__name__}: {e}"
+        notes = []
+        for source in ("nvml", "nvml-ctypes"):
+            try:
+                if source == "nvml":
+                    import pynvml as nvml
+                else:
+                    nvml = CtypesNvml()
+                self._start_nvml(nvml, source)
+                return self
+            except Exception as e:  # noqa: BLE001
+                notes.append(f"{source}: {type(e).__name__}: {e}")
+        self.error = "; ".join(notes)
         try:
             import subprocess
             self._first = threading.Event()
@@ -191,7 +251,7 @@ class ClockSampler:
                 self._proc.kill()
         if self._thread is not None:
             self._thread.join(timeout=2)
-        if self.source == "nvml" and not self.samples:
+        if self.source.startswith("nvml") and not self.samples:
             self._nvml_once()
         return False
 

@@ -7,6 +7,7 @@ import subprocess
 import sys
 
 import bench
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -83,3 +84,47 @@ def test_traffic_record_is_used_only_for_the_source_it_was_taken_on(tmp_path, mo
         {"prefill_swa_stream_kernel": dict(entry, source_sha=bench.source_sha(rel))}))
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench.ncu_traffic(rel, "prefill_swa_stream_kernel") is None
+
+
+class _FakeNvmlLib:
+    """The NVML C entry points the ctypes reader calls, answering like a GPU at
+    1965 of 2032 MHz under a power cap."""
+
+    def nvmlInit_v2(self):
+        return 0
+
+    def nvmlDeviceGetHandleByIndex_v2(self, index, handle_ref):
+        handle_ref._obj.value = 1234
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, handle, kind, out_ref):
+        out_ref._obj.value = 1965
+        return 0
+
+    def nvmlDeviceGetMaxClockInfo(self, handle, kind, out_ref):
+        out_ref._obj.value = 2032
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, handle, out_ref):
+        out_ref._obj.value = 0x4 | 0x1   # sw power cap + idle
+        return 0
+
+
+def test_clock_sampler_reads_nvml_through_ctypes():
+    nvml = bench.CtypesNvml(lib=_FakeNvmlLib())
+    s = bench.ClockSampler(0)
+    s._start_nvml(nvml, "nvml-ctypes")
+    s._stop.set()
+    s._thread.join(timeout=2)
+    s._nvml_once()
+    out = s.summary()
+    assert out["source"] == "nvml-ctypes" and out["sm_max_mhz"] == 2032.0
+    assert out["sm_mhz"] == 1965.0 and out["reasons"] == ["sw_power_cap"]
+
+
+def test_ctypes_nvml_raises_on_an_error_code():
+    class Bad(_FakeNvmlLib):
+        def nvmlInit_v2(self):
+            return 9   # NVML_ERROR_DRIVER_NOT_LOADED
+    with pytest.raises(RuntimeError):
+        bench.CtypesNvml(lib=Bad()).nvmlInit()
