@@ -14,24 +14,29 @@
 //
 // Three kernels, none with atomics on the gradients:
 //   bwd_pre_kernel   D_i per (b, h, i) and a block-reduced dsigma;
-//   bwd_dkdv_kernel  one CTA per (128-key tile, kv head, b).  The key tile is
-//                    the MMA's M side: per step of 64 query rows of one head
-//                    of the group, S^T = K Q^T and dP^T = V dO^T go to TMEM
-//                    (tcgen05.mma, K and Q / V and dO from shared memory);
-//                    two compute warpgroups (alternate steps, one key row per
-//                    thread) form P^T and dS^T = P^T (dP^T - D) in bf16 over
-//                    the same TMEM columns; then dV += P^T dO and
-//                    dK += dS^T Q run with A from TMEM.  dK and dV stay in
-//                    TMEM for the whole CTA;
-//   bwd_dq_kernel    one CTA per (128-row query tile, head, b), the query rows
-//                    on the M side.  The epilogue warps copy the tile's Q and
+//   bwd_dkdv_kernel  persistent CTAs (one per SM) over items (128-key tile,
+//                    kv head, b).  The key tile is the MMA's M side: per
+//                    step of 64 query rows of one head of the group,
+//                    S^T = K Q^T and dP^T = V dO^T go to TMEM (tcgen05.mma,
+//                    K and Q / V and dO from shared memory); two compute
+//                    warpgroups (alternate steps, one key row per thread)
+//                    form P^T and dS^T = P^T (dP^T - D) in bf16 over the same
+//                    TMEM columns; then dV += P^T dO and dK += dS^T Q run
+//                    with A from TMEM.  dK and dV stay in TMEM for the whole
+//                    item, and an epilogue warpgroup drains them;
+//   bwd_dq_kernel    persistent CTAs over items (128-row query tile, head,
+//                    b), the query rows on the M side.  The epilogue warps copy the tile's Q and
 //                    dO rows into TMEM, so per step of 64 keys S = Q K^T and
 //                    dP = dO V^T take A from TMEM and read only K and V from
 //                    shared memory; dS = P (dP - D) in bf16 in TMEM, then
 //                    dQ += dS K with A from TMEM.
-// Q, dO, K and V tiles arrive by TMA (128-byte swizzle) through 3-stage rings
-// fed by one producer warp; one thread issues every MMA; S/dP sit in two TMEM
-// buffers so one step's exponentials overlap the next step's products.
+// Q, dO, K and V tiles arrive by TMA (128-byte swizzle) through 4-stage
+// (dK/dV) and 3-stage (dQ) rings fed by one producer warp; one thread issues
+// every MMA; S/dP sit in two TMEM buffers so one step's exponentials overlap
+// the next step's products.  The compute warps keep their instruction count
+// low (paired fp32 arithmetic, the column mask only where a row does not see
+// the whole step, no register spills): work in warps beside the tensor-core
+// stream slows that stream.
 // P and dS are rounded to bf16 before the products that use them, as the
 // forward rounds P.  Computing dQ in its own kernel repeats S and dP (seven
 // products per visible pair instead of five) but keeps the gradients free of
